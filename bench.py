@@ -1,0 +1,454 @@
+"""Benchmark of the Mamba2 SSD hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input shaped like a
+Mamba2-130M layer: the chunked scan over 2 sequences x 2048 tokens (H=24, P=64, G=1,
+N=128, chunk 256, bf16 activations, fp32 initial states), the gated RMSNorm of its output
+(d_inner 1536, one group), and one decode token for both requests through the pooled
+state update.  Inputs are resident in HBM; L2 (129 MB, larger than the step's inputs) is
+flushed by writing a 512 MB buffer between timed steps, outside the timed events.
+
+Prints one JSON line (rank 0).  Also measured in the same run and reported as extra keys:
+the decode state update on a 512-slot [128, 64, 128] fp32 pool at batch 256 (HBM GB/s),
+and the scan on the Nemotron-H-shaped varlen prefill (16384 tokens, H=128, G=8).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (double precision, host cores) on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "mamba2_130m"
+METRIC = "Mamba2 SSD prefill tokens/s; decode state-update HBM GB/s vs peak"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def scan_bytes(T, H, P, G, N, nseq, init=True, final=True, act_bytes=2):
+    """Algorithmic HBM bytes of one scan launch: x and y, B and C, dt, per-head params,
+    initial and final states (intermediate chunk states are not counted)."""
+    b = T * H * P * act_bytes * 2 + T * G * N * act_bytes * 2 + T * H * 4 + H * 4 * 3
+    b += (nseq + 1) * 4
+    if init:
+        b += nseq * H * P * N * 4
+    if final:
+        b += nseq * H * P * N * 4
+    return b
+
+
+def update_bytes(active, batch, H, P, G, N, act_bytes=2):
+    """Algorithmic HBM bytes of one decode launch: each active slot's state read and
+    written once, plus x, y, B, C, dt of every row and the per-head parameters."""
+    return (active * H * P * N * 4 * 2 + batch * (2 * H * P * act_bytes + 2 * G * N * act_bytes
+                                                  + H * 4 + 4) + H * 4 * 3)
+
+
+def norm_bytes(rows, d, act_bytes=2, w_bytes=2):
+    return rows * d * act_bytes * 3 + d * w_bytes
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from mamba2_ssd_state_gb300 import build as lib_build
+    from mamba2_ssd_state_gb300 import inputs as I
+    from mamba2_ssd_state_gb300 import ssd
+
+    lib_build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    hbm_peak, tc_peak, peak_kind = load_peaks()
+
+    def T_(t):
+        dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
+        return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
+
+    w = I.WORKLOADS[WORKLOAD]
+    s = I.scan_workload(WORKLOAD)
+    H, P, G, N, T, nseq = s.H, s.P, s.G, s.N, s.T, s.nseq
+    d = H * P
+    x, dt, A, B, C, Dp, bias = (T_(s.x), T_(s.dt), T_(s.A), T_(s.B), T_(s.C), T_(s.D),
+                                T_(s.dt_bias))
+    init = T_(s.initial_states)
+    cu = torch.from_numpy(s.cu_seqlens).to(dev)
+    nrm = I.make_norm_inputs(T, d, w["norm_group"], act="bf16", seed=w["seed"] + 50)
+    z, wt = T_(nrm.z), T_(nrm.weight)
+    y = torch.empty((T, H, P), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((nseq, H, P, N), dtype=torch.float32, device=dev)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    # decode of both requests after their prefill: slots 0 and 1 of a 2-slot pool
+    pool = torch.zeros((nseq, H, P, N), dtype=torch.float32, device=dev)
+    upd = I.make_update_inputs(nseq, list(range(nseq)), H, P, G, N, act="bf16",
+                               seed=w["seed"] + 60)
+    ux, udt, uB, uC = T_(upd.x), T_(upd.dt), T_(upd.B), T_(upd.C)
+    uidx = torch.arange(nseq, dtype=torch.int32, device=dev)
+    uy = torch.empty((nseq, H, P), dtype=torch.bfloat16, device=dev)
+    status = ssd.new_status(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp,
+                       dt_bias=bias, initial_states=init, y=y, final_states=fs, status=status)
+        if ev:
+            ev[1].record(stream)
+        ssd.gated_rmsnorm(y.view(T, d), z, wt, group_size=w["norm_group"], eps=1e-5, out=out)
+        if ev:
+            ev[2].record(stream)
+        ssd.state_update(pool, uidx, ux, udt, A, uB, uC, D=Dp, dt_bias=bias, y=uy,
+                         status=status)
+        if ev:
+            ev[3].record(stream)
+
+    launches_per_step = 3
+    for i in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+        if i == 0:
+            pool.copy_(fs)   # the decode continues the two requests just prefilled
+    torch.cuda.synchronize()
+    rc, bits = ssd.read_status(status)
+    if bits:
+        raise RuntimeError(f"device status bits {bits} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()          # L2 flush, outside the step's events
+        step(evs[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    ck = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    scan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    norm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    upd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_per_step = T + nseq
+    value = tokens_per_step * world * args.steps / (total_ms / 1e3)
+
+    sbytes = scan_bytes(T, H, P, G, N, nseq)
+    scan_avg = sum(scan_ms) / len(scan_ms)
+    roof = {"bound": "hbm", "kernel": "scan_tc_kernel", "achieved": sbytes / (scan_avg / 1e3) / 1e9,
+            "peak": hbm_peak, "unit": "GB/s", "peak_kind": f"{peak_kind} hbm copy",
+            "algorithmic_bytes_per_launch": sbytes, "avg_launch_us": scan_avg * 1e3,
+            "traffic": None}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    nb = norm_bytes(T, d)
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind)
+
+    # end to end through the public API: inputs from pinned host memory, result back
+    host_in = {k: v.detach().cpu().pin_memory() for k, v in
+               dict(x=x, dt=dt, B=B, C=C, init=init, z=z, ux=ux, udt=udt, uB=uB, uC=uC).items()}
+    host_out = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k2, v in host_in.items():
+            dev_in[k2].copy_(v, non_blocking=True)
+        ssd.chunk_scan(dev_in["x"], dev_in["dt"], A, dev_in["B"], dev_in["C"], cu_seqlens=cu,
+                       chunk_size=s.chunk_size, D=Dp, dt_bias=bias, initial_states=dev_in["init"],
+                       y=y, final_states=fs, status=status)
+        ssd.gated_rmsnorm(y.view(T, d), dev_in["z"], wt, group_size=w["norm_group"], out=out)
+        ssd.state_update(pool, uidx, dev_in["ux"], dev_in["udt"], A, dev_in["uB"], dev_in["uC"],
+                         D=Dp, dt_bias=bias, y=uy, status=status)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens_per_step * world * args.steps / (e2e_ms / 1e3)
+
+    rc, bits = ssd.read_status(status)
+    if bits:
+        raise RuntimeError(f"device status bits {bits} after the timed region")
+
+    if rank != 0:
+        return None
+    cpu = None if args.no_cpu else cpu_baseline(s, nrm, w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Mamba2-130M-shaped layer: 2 x 2048 tokens, H=24 P=64 G=1 "
+                               "N=128, chunk 256, scan + gated RMSNorm (d 1536) + decode of "
+                               "both requests", "seqlens": s.seqlens, "H": H, "P": P, "G": G,
+                   "N": N, "chunk_size": s.chunk_size, "tokens_per_step": tokens_per_step,
+                   "l2": "flushed between steps (512 MB write, outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "breakdown_us": {"scan": scan_avg * 1e3, "gated_rmsnorm": 1e3 * sum(norm_ms) / len(norm_ms),
+                         "state_update": 1e3 * sum(upd_ms) / len(upd_ms)},
+        "wall_s_timed_region": t_wall,
+        "roofline": roof,
+        "gated_rmsnorm_gbs": nb / (sum(norm_ms) / len(norm_ms) / 1e3) / 1e9,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": ck,
+        "cpu_baseline": cpu,
+    }
+    line.update(extra)
+    return line
+
+
+def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
+    """Decode at batch 256 on the 512-slot pool, and the large varlen prefill scan."""
+    res = {}
+    stream = torch.cuda.current_stream()
+    H, P, G, N, S, batch = 128, 64, 8, 128, 512, 256
+    idx = I.padded_permutation(S, batch, seed=3000 + batch)
+    u = I.make_update_inputs(1, idx, H, P, G, N, act="bf16", seed=3100 + batch,
+                             pool_values=np.zeros((1, H, P, N), np.float32))
+
+    def T_(t):
+        dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
+        return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
+
+    pool = torch.randn((S, H, P, N), device=dev, dtype=torch.float32)
+    args = (pool, torch.from_numpy(idx).to(dev), T_(u.x), T_(u.dt), T_(u.A), T_(u.B), T_(u.C))
+    kw = dict(D=T_(u.D), dt_bias=T_(u.dt_bias))
+    for _ in range(3):
+        ssd.state_update(*args, **kw)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        ssd.state_update(*args, **kw)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / iters
+    active = int((idx >= 0).sum())
+    ub = update_bytes(active, batch, H, P, G, N)
+    res["decode_state_update"] = {
+        "workload": "512-slot pool of [128,64,128] fp32 states, batch 256, 10% rows -1 "
+                    "(pool > L2)", "active_slots": active, "avg_launch_us": us,
+        "algorithmic_bytes_per_launch": ub, "achieved_gbs": ub / (us / 1e6) / 1e9,
+        "peak_gbs": hbm_peak, "frac": ub / (us / 1e6) / 1e9 / hbm_peak,
+        "peak_kind": f"{peak_kind} hbm copy"}
+    del pool, args
+    # large varlen prefill
+    s = I.scan_workload("nemotron_h_varlen")
+    tens = [T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D, s.dt_bias, s.initial_states)]
+    x, dt, A, B, C, Dp, bias, init = tens
+    hi = torch.from_numpy(s.has_initial_state).to(dev)
+    cu = torch.from_numpy(s.cu_seqlens).to(dev)
+    y = torch.empty_like(x)
+    fs = torch.empty((s.nseq, s.H, s.P, s.N), dtype=torch.float32, device=dev)
+
+    def run():
+        ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp, dt_bias=bias,
+                       initial_states=init, has_initial_state=hi, y=y, final_states=fs)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / iters
+    sb = scan_bytes(s.T, s.H, s.P, s.G, s.N, s.nseq)
+    res["scan_nemotron_h_varlen"] = {
+        "workload": "4 packed sequences [8192,3000,517,4675], H=128 P=64 G=8 N=128, chunk 128 "
+                    "(inputs 0.6 GB > L2)", "tokens_per_s": s.T / (us / 1e6),
+        "avg_launch_us": us, "algorithmic_bytes_per_launch": sb,
+        "achieved_gbs": sb / (us / 1e6) / 1e9, "frac_hbm": sb / (us / 1e6) / 1e9 / hbm_peak}
+    return res
+
+
+# ----------------------------------------------------------------------------- oracle
+
+def cpu_baseline(s, nrm, w, budget_s=12.0):
+    """The oracle as it stands, on the host cores: the same workload's scan + norm +
+    decode, repeated while under the time budget (at least once)."""
+    import oracle
+
+    cores = os.cpu_count()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.scan_seq(s.x.values, s.dt.values, s.A.values, s.B.values, s.C.values, D=s.D.values,
+                        dt_bias=s.dt_bias.values, initial_states=s.initial_states.values,
+                        cu_seqlens=s.cu_seqlens)
+        oracle.gated_rmsnorm(np.zeros((s.T, s.H * s.P), np.float32), nrm.z.values,
+                             nrm.weight.values, group_size=w["norm_group"])
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 50:
+            break
+    el = time.perf_counter() - t0
+    return {"value": reps * s.T / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full step(s) of the same workload (scan + norm), "
+                      f"double precision, OpenMP over (sequence, head)",
+            "seconds": el}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from mamba2_ssd_state_gb300 import inputs as I
+    import oracle
+    from oracle import build as ob
+
+    ob.build()
+    w = I.WORKLOADS[WORKLOAD]
+    s = I.scan_workload(WORKLOAD)
+    nrm = I.make_norm_inputs(s.T, s.H * s.P, w["norm_group"], act="bf16", seed=w["seed"] + 50)
+    # bounded sample per step: one of the two sequences (2048 tokens) through scan + norm
+    L = s.seqlens[0]
+    sl = slice(0, L)
+
+    def step():
+        oracle.scan_seq(s.x.values[sl], s.dt.values[sl], s.A.values, s.B.values[sl],
+                        s.C.values[sl], D=s.D.values, dt_bias=s.dt_bias.values,
+                        initial_states=s.initial_states.values[:1])
+        oracle.gated_rmsnorm(np.zeros((L, s.H * s.P), np.float32), nrm.z.values[sl],
+                             nrm.weight.values, group_size=w["norm_group"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    v = L * args.steps / el
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Mamba2-130M-shaped layer (one 2048-token sequence of the "
+                                   "2 x 2048 batch per step), scan + gated RMSNorm"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": "one 2048-token sequence per step"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-extra", action="store_true", help="skip the decode / large-scan legs")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

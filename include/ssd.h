@@ -1,0 +1,214 @@
+/*
+ * ssd.h -- C ABI of libssd.so: the three Mamba2 SSD ops on an NVIDIA GB300 (sm_103a).
+ *
+ * Sources cited below:
+ *   [vllm.cpp #566] the pull-request page "W2 finish (KERNEL-SSM-MAMBA): 9/9 CUDA
+ *       mutations caught, compute-sanitizer clean, Debug arm green, spec 8.3
+ *       re-authored (#496)", with the squash-merge message of its successor #675
+ *       printed on the same page.  It names the ops vt::Mamba2ChunkScan,
+ *       vt::Mamba2StateUpdate and vt::RmsNormGatedGroup, their arguments (through its
+ *       mutation table, section "Evidence") and the device-arm policies (sections
+ *       "Carried forward" and the #675 message).
+ *   [atlas #69] the pull-request page "feat(spark-server): inject tool-call parser
+ *       system prompt" (atlas PR #69), whose SsmStatePool keeps one fp32 SSM state
+ *       slot per concurrent decode request.
+ *   [Mamba-2] Dao & Gu, "Transformers are SSMs" (2024), the SSD layer, for the
+ *       recurrence itself, which the pages name but do not print.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is DEVICE memory owned by the caller, except the args
+ *     structs themselves (host).  The library keeps no pointer after it returns and
+ *     allocates no memory: no cudaMalloc, no workspace.
+ *   - Every call is asynchronous on the caller's stream (a cudaStream_t passed as
+ *     ssd_stream_t; NULL = the legacy default stream).  Nothing is copied device to
+ *     host and no call synchronises, except ssd_read_status.
+ *   - Errors the host can see (NULL required pointer, bad size, unsupported dtype or
+ *     shape) are returned before anything is launched.  Errors only the device can
+ *     see (A not negative, slot index out of range, malformed cu_seqlens) are OR-ed as
+ *     SSD_DEV_* bits into the caller's optional uint32 status word with atomicOr; the
+ *     offending unit of work is skipped, never trapped, and its outputs are zero.  This
+ *     follows [vllm.cpp #566] "Carried forward" (the device arm does no D2H per call)
+ *     and the #675 message (index clamps instead of out-of-bounds accesses).
+ *   - Layouts are row-major and dense unless a stride argument says otherwise.
+ *     Activations are bf16 or fp32 (ssd_dtype); dt, dt_bias, A, D and all states are
+ *     fp32.
+ */
+#ifndef SSD_H
+#define SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+typedef struct CUstream_st* ssd_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1,    /* NULL required pointer, negative or inconsistent size */
+  SSD_ERR_UNSUPPORTED = 2,    /* a valid request this build has no kernel for */
+  SSD_ERR_A_NOT_NEGATIVE = 3, /* ssd_read_status: device saw A[h] not < 0 */
+  SSD_ERR_INDEX = 4,          /* ssd_read_status: device saw a slot index out of range */
+  SSD_ERR_SEQ_META = 5,       /* ssd_read_status: device saw malformed cu_seqlens */
+  SSD_ERR_CUDA = 6,           /* a CUDA runtime call failed (launch, attribute, ...) */
+  SSD_ERR_TIMEOUT = 7         /* ssd_read_status: a kernel pipeline wait ran out (bug guard) */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Bits the kernels OR into the caller's device status word. */
+#define SSD_DEV_A_NOT_NEG 0x1u
+#define SSD_DEV_INDEX_OOR 0x2u
+#define SSD_DEV_SEQ_META 0x4u
+#define SSD_DEV_TIMEOUT 0x8u /* a bounded pipeline wait gave up; outputs are incomplete */
+
+/* Scan implementation selector (ssd_scan_args.impl). */
+#define SSD_IMPL_AUTO 0  /* tensor-core path when the shape allows it, else SIMT */
+#define SSD_IMPL_SIMT 1  /* token-sequential fp32 SIMT kernel (any supported shape) */
+#define SSD_IMPL_TC 2    /* tcgen05/TMEM + TMA chunked kernel; UNSUPPORTED if not possible */
+
+/* ------------------------------------------------------------------------------------
+ * ssd_chunk_scan -- Mamba2 chunked SSD scan (prefill), vt::Mamba2ChunkScan of
+ * [vllm.cpp #566], over variable-length sequences packed along the token axis.
+ *
+ * Per sequence s (tokens cu_seqlens[s] .. cu_seqlens[s+1]-1), head h, group
+ * g = h / (H/G), channel p < P and state index n < N ([Mamba-2]):
+ *   dt_t      = softplus(dt[t,h] + dt_bias[h])     (dt_softplus != 0; else the plain sum)
+ *   h_t[p,n]  = exp(dt_t * A[h]) * h_{t-1}[p,n] + dt_t * B[t,g,n] * x[t,h,p]
+ *   y[t,h,p]  = sum_n C[t,g,n] * h_t[p,n] + D[h] * x[t,h,p]      (the D skip)
+ *   h_{-1}    = initial_states[s] if initial_states != NULL and has_initial_state[s]
+ *               (NULL has_initial_state = every sequence has one), else 0
+ *   final_states[s] = h at the sequence's last token (the initial state when empty).
+ * The chunked evaluation splits each sequence into chunks of chunk_size tokens starting
+ * at its first token (segsum decay, C.B^T, chunk states, state passing with
+ * states[c-1] feeding chunk c, output contractions); the mutation table of
+ * [vllm.cpp #566] section "Evidence" (M1-M4) names those parts.  Exact arithmetic
+ * gives the sequential result for every chunk_size.
+ *
+ * Arguments (struct, host memory; set struct_size = sizeof(ssd_scan_args)):
+ *   x [T, H, P] act_dtype, token stride x_stride_t elements (0 = H*P)
+ *   dt [T, H] fp32 (token stride H); dt_bias [H] fp32 or NULL (= 0); A [H] fp32, must
+ *     be < 0 (else SSD_DEV_A_NOT_NEG and that head's outputs are zero); D [H] fp32 or
+ *     NULL (= 0)
+ *   B, C [T, G, N] act_dtype, token strides B_stride_t / C_stride_t elements (0 = G*N)
+ *   initial_states [nseq, H, P, N] fp32 or NULL; has_initial_state [nseq] uint8 or NULL
+ *   cu_seqlens [nseq + 1] int32, device: 0 = cu[0] <= cu[1] <= ... <= cu[nseq] = T
+ *     (violations set SSD_DEV_SEQ_META; offending sequences produce nothing)
+ *   y [T, H, P] act_dtype, dense (written); final_states [nseq, H, P, N] fp32 or NULL
+ *   chunk_size: 1 .. 256 (the tensor-core path takes 64, 128 or 256)
+ *   impl: SSD_IMPL_*; p_block: 0 = choose, else the channel split of the tensor-core
+ *     path (16, 32 or 64; must divide P)
+ *   d_status: uint32 device word or NULL
+ * Shapes: H % G == 0; SIMT path N <= 256; tensor-core path bf16, N == 128,
+ * P % 16 == 0, 16-byte aligned rows.  Outputs must not alias inputs.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  uint32_t struct_size;
+  const void* x;
+  int64_t x_stride_t;
+  const float* dt;
+  const float* dt_bias;
+  int32_t dt_softplus;
+  const float* A;
+  const float* D;
+  const void* B;
+  int64_t B_stride_t;
+  const void* C;
+  int64_t C_stride_t;
+  const float* initial_states;
+  const uint8_t* has_initial_state;
+  const int32_t* cu_seqlens;
+  int32_t nseq, T, H, P, G, N, chunk_size;
+  ssd_dtype act_dtype;
+  void* y;
+  float* final_states;
+  uint32_t* d_status;
+  int32_t impl;
+  int32_t p_block;
+} ssd_scan_args;
+
+SSD_API ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_state_update -- one decode token per request on a pooled state cache,
+ * vt::Mamba2StateUpdate of [vllm.cpp #566]; the pool is [atlas #69]'s SsmStatePool
+ * layout, one fp32 [H, P, N] slot per concurrent request.
+ *
+ * For each batch row b with slot s = state_indices[b]:
+ *   s == -1 (the NULL row of mutation M6): no slot is read or written; y[b] = 0.
+ *   s < -1 or s >= num_slots: SSD_DEV_INDEX_OOR; no slot touched; y[b] = 0.
+ *   else, per head h with A[h] < 0 (a sign test: -1e-30 passes, +0, -0 and NaN do not;
+ *   failing heads set SSD_DEV_A_NOT_NEG, keep their slot state and get y = 0):
+ *     a = exp(dt_b * A[h]),  dt_b = softplus(dt[b,h] + dt_bias[h])
+ *     pool[s,h,p,n] = a * pool[s,h,p,n] + dt_b * B[b,g,n] * x[b,h,p]
+ *     y[b,h,p]      = sum_n C[b,g,n] * pool[s,h,p,n] + D[h] * x[b,h,p]
+ * Slots not named by an active row are never touched (bit-identical).  Two rows naming
+ * the same slot is a caller error (the result is undefined; nothing faults).
+ *
+ *   state_pool [num_slots, H, P, N] fp32, slot stride slot_stride elements (0 = H*P*N)
+ *   state_indices [batch] int32; x [batch, H, P] act; dt [batch, H] fp32; dt_bias [H]
+ *   or NULL; A [H]; B, C [batch, G, N] act; D [H] or NULL; y [batch, H, P] act.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  uint32_t struct_size;
+  float* state_pool;
+  int64_t slot_stride;
+  int32_t num_slots;
+  const int32_t* state_indices;
+  int32_t batch;
+  const void* x;
+  const float* dt;
+  const float* dt_bias;
+  int32_t dt_softplus;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  void* y;
+  int32_t H, P, G, N;
+  ssd_dtype act_dtype;
+  uint32_t* d_status;
+} ssd_update_args;
+
+SSD_API ssd_status ssd_state_update(const ssd_update_args* args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * gated_rmsnorm -- silu-gated RMSNorm with per-group variance, vt::RmsNormGatedGroup of
+ * [vllm.cpp #566] (mutations M7 "whole-row variance, not per-group" and M8 "sigmoid
+ * instead of silu" fix its two parts).  The gate is applied first:
+ *   g   = x * silu(z),  silu(z) = z / (1 + exp(-z))      (z == NULL: g = x)
+ *   out = g / sqrt(mean(g^2 over the group) + eps) * weight
+ * Groups are group_size contiguous channels of each row; d % group_size == 0.
+ *   x, z, out [rows, d] act (dense; out may alias x); weight [d] wt.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status gated_rmsnorm(const void* x, const void* z, const void* weight, void* out,
+                         int64_t rows, int32_t d, int32_t group_size, float eps,
+                         ssd_dtype act, ssd_dtype wt, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_read_status -- the one synchronising helper: waits for `stream`, reads the
+ * device status word, optionally clears it, and maps the first set bit to an
+ * ssd_status (A_NOT_NEG before INDEX before SEQ_META before TIMEOUT).  *bits_out (may be NULL)
+ * receives the raw bits.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status ssd_read_status(uint32_t* d_status, int32_t clear, uint32_t* bits_out,
+                           ssd_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+SSD_API const char* ssd_status_string(ssd_status st);
+
+/* Library version (major*10000 + minor*100 + patch). */
+SSD_API int32_t ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_H */

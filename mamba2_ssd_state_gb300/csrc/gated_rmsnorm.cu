@@ -1,0 +1,181 @@
+// gated_rmsnorm.cu -- silu-gated RMSNorm with per-group variance (vt::RmsNormGatedGroup of
+// the vllm.cpp page "W2 finish (KERNEL-SSM-MAMBA)"; its mutation rows M7 "whole-row
+// variance, not per-group" and M8 "sigmoid instead of silu" fix the two parts).
+//
+//   g = x * silu(z);  out = g * rsqrt(mean_group(g^2) + eps) * w
+//
+// HBM-bound: x and z are read once and out written once (6 bytes per element in bf16).
+// One warp owns one (row, group); in the vector path every lane keeps its
+// VPT * 8 gated values in registers between the reduction and the write, so the op is a
+// single pass over memory with 16-byte loads and stores and a warp-shuffle reduction.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// 8 activations per 16-byte vector (bf16) or two float4 (fp32).
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float v[8]) {
+    uint4 t = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float v[8]) {
+    uint4 t;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = t;
+  }
+};
+template <> struct Vec8<float> {
+  static __device__ __forceinline__ void load(const float* p, float v[8]) {
+    float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float v[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+
+// group_size == VPT * 256: lane l holds elements [8 (l + 32 i), +8) for i < VPT, so each
+// load instruction of a warp covers 32 consecutive 8-element vectors (coalesced).
+template <typename TA, typename TW, int VPT>
+__global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
+                                                       const TA* __restrict__ z,
+                                                       const TW* __restrict__ w, TA* out,
+                                                       int64_t units, int d, int gs, float eps) {
+  const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (unit >= units) return;
+  const int lane = threadIdx.x & 31;
+  const int ngroups = d / gs;
+  const int64_t row = unit / ngroups;
+  const int col0 = (int)(unit % ngroups) * gs;
+  const size_t base = (size_t)row * d + col0;
+  float g[VPT][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int off = 8 * (lane + 32 * i);
+    float xv[8];
+    Vec8<TA>::load(x + base + off, xv);
+    if (z) {
+      float zv[8];
+      Vec8<TA>::load(z + base + off, zv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[i][e] = xv[e] * silu(zv[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[i][e] = xv[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(g[i][e], g[i][e], ss);
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)gs + eps);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int off = 8 * (lane + 32 * i);
+    float wv[8], o[8];
+    Vec8<TW>::load(w + col0 + off, wv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = g[i][e] * r * wv[e];
+    Vec8<TA>::store(out + base + off, o);
+  }
+}
+
+// Any group size: one warp per (row, group), two passes (the second re-reads x and z,
+// which are still in L1/L2 for the group just reduced).
+template <typename TA, typename TW>
+__global__ void __launch_bounds__(256) norm_generic_kernel(const TA* x,
+                                                           const TA* __restrict__ z,
+                                                           const TW* __restrict__ w, TA* out,
+                                                           int64_t units, int d, int gs,
+                                                           float eps) {
+  const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (unit >= units) return;
+  const int lane = threadIdx.x & 31;
+  const int ngroups = d / gs;
+  const int64_t row = unit / ngroups;
+  const int col0 = (int)(unit % ngroups) * gs;
+  const size_t base = (size_t)row * d + col0;
+  float ss = 0.f;
+  for (int k = lane; k < gs; k += 32) {
+    float gv = to_f32(x[base + k]);
+    if (z) gv *= silu(to_f32(z[base + k]));
+    ss = fmaf(gv, gv, ss);
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)gs + eps);
+  for (int k = lane; k < gs; k += 32) {
+    float gv = to_f32(x[base + k]);
+    if (z) gv *= silu(to_f32(z[base + k]));
+    out[base + k] = from_f32<TA>(gv * r * to_f32(w[col0 + k]));
+  }
+}
+
+template <typename TA, typename TW>
+cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out, int64_t rows,
+                         int d, int gs, float eps, cudaStream_t st) {
+  const int64_t units = rows * (int64_t)(d / gs);
+  const int64_t blocks = (units + 7) / 8;
+  const TA* xp = static_cast<const TA*>(x);
+  const TA* zp = static_cast<const TA*>(z);
+  const TW* wp = static_cast<const TW*>(w);
+  TA* op = static_cast<TA*>(out);
+  const bool aligned = ((uintptr_t)x % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
+                       (z == nullptr || (uintptr_t)z % 16 == 0) && ((uintptr_t)w % 16 == 0) &&
+                       ((size_t)d * sizeof(TA)) % 16 == 0;
+  const int vpt = (aligned && gs % 256 == 0) ? gs / 256 : 0;
+#define SSD_NORM_CASE(V)                                                                   \
+  case V:                                                                                  \
+    norm_vec_kernel<TA, TW, V><<<(unsigned)blocks, 256, 0, st>>>(xp, zp, wp, op, units, d, \
+                                                                 gs, eps);                 \
+    break;
+  switch (vpt) {
+    SSD_NORM_CASE(1)
+    SSD_NORM_CASE(2)
+    SSD_NORM_CASE(3)
+    SSD_NORM_CASE(4)
+    SSD_NORM_CASE(5)
+    SSD_NORM_CASE(6)
+    SSD_NORM_CASE(8)
+    default:
+      norm_generic_kernel<TA, TW><<<(unsigned)blocks, 256, 0, st>>>(xp, zp, wp, op, units, d,
+                                                                    gs, eps);
+  }
+#undef SSD_NORM_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, void* out,
+                                 int64_t rows, int d, int gs, float eps, ssd_dtype act,
+                                 ssd_dtype wt, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  if (act == SSD_BF16)
+    return wt == SSD_BF16
+               ? launch_typed<__nv_bfloat16, __nv_bfloat16>(x, z, w, out, rows, d, gs, eps, st)
+               : launch_typed<__nv_bfloat16, float>(x, z, w, out, rows, d, gs, eps, st);
+  return wt == SSD_BF16 ? launch_typed<float, __nv_bfloat16>(x, z, w, out, rows, d, gs, eps, st)
+                        : launch_typed<float, float>(x, z, w, out, rows, d, gs, eps, st);
+}
+
+}  // namespace ssd

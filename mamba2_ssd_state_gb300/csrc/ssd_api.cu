@@ -1,0 +1,124 @@
+// ssd_api.cu -- the C ABI of libssd.so (declared in include/ssd.h): host-side argument
+// validation and kernel dispatch.  Nothing here computes any part of the ops; every
+// step runs in the kernels of the other translation units.
+#include <cstring>
+
+#include "ssd_internal.cuh"
+
+using namespace ssd;
+
+namespace {
+
+inline bool bad_dtype(ssd_dtype d) { return d != SSD_F32 && d != SSD_BF16; }
+
+ssd_status validate_scan(const ssd_scan_args* a) {
+  if (!a || a->struct_size < sizeof(ssd_scan_args)) return SSD_ERR_INVALID_ARG;
+  if (!a->A || !a->cu_seqlens) return SSD_ERR_INVALID_ARG;
+  if (a->T > 0 && (!a->x || !a->dt || !a->B || !a->C || !a->y)) return SSD_ERR_INVALID_ARG;
+  if (a->nseq < 1 || a->T < 0 || a->H < 1 || a->P < 1 || a->G < 1 || a->N < 1)
+    return SSD_ERR_INVALID_ARG;
+  if (a->H % a->G != 0) return SSD_ERR_INVALID_ARG;
+  if (a->chunk_size < 1 || a->chunk_size > 256) return SSD_ERR_INVALID_ARG;
+  if (bad_dtype(a->act_dtype)) return SSD_ERR_INVALID_ARG;
+  if (a->x_stride_t != 0 && a->x_stride_t < (int64_t)a->H * a->P) return SSD_ERR_INVALID_ARG;
+  if (a->B_stride_t != 0 && a->B_stride_t < (int64_t)a->G * a->N) return SSD_ERR_INVALID_ARG;
+  if (a->C_stride_t != 0 && a->C_stride_t < (int64_t)a->G * a->N) return SSD_ERR_INVALID_ARG;
+  if (a->impl < SSD_IMPL_AUTO || a->impl > SSD_IMPL_TC) return SSD_ERR_INVALID_ARG;
+  if (a->p_block != 0 && a->p_block != 16 && a->p_block != 32 && a->p_block != 64)
+    return SSD_ERR_INVALID_ARG;
+  if (a->nseq > 65535 || a->H > 65535) return SSD_ERR_UNSUPPORTED;  // grid limits
+  return SSD_OK;
+}
+
+ssd_status validate_update(const ssd_update_args* a) {
+  if (!a || a->struct_size < sizeof(ssd_update_args)) return SSD_ERR_INVALID_ARG;
+  if (!a->state_pool || !a->A) return SSD_ERR_INVALID_ARG;
+  if (a->batch > 0 &&
+      (!a->state_indices || !a->x || !a->dt || !a->B || !a->C || !a->y))
+    return SSD_ERR_INVALID_ARG;
+  if (a->num_slots < 1 || a->batch < 0 || a->H < 1 || a->P < 1 || a->G < 1 || a->N < 1)
+    return SSD_ERR_INVALID_ARG;
+  if (a->H % a->G != 0) return SSD_ERR_INVALID_ARG;
+  if (bad_dtype(a->act_dtype)) return SSD_ERR_INVALID_ARG;
+  if (a->slot_stride != 0 && a->slot_stride < (int64_t)a->H * a->P * a->N)
+    return SSD_ERR_INVALID_ARG;
+  if (a->batch > 65535) return SSD_ERR_UNSUPPORTED;  // grid limit
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream) {
+  ssd_status v = validate_scan(args);
+  if (v != SSD_OK) return v;
+  const ssd_scan_args& a = *args;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int pb = 0;
+  const bool tc_ok = scan_tc_supported(a, &pb);
+  if (a.impl == SSD_IMPL_TC || (a.impl == SSD_IMPL_AUTO && tc_ok)) {
+    if (!tc_ok) return SSD_ERR_UNSUPPORTED;
+    return launch_scan_tc(a, pb, st);
+  }
+  if (a.N > 256) return SSD_ERR_UNSUPPORTED;
+  return launch_scan_simt(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_state_update(const ssd_update_args* args, ssd_stream_t stream) {
+  ssd_status v = validate_update(args);
+  if (v != SSD_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_state_update(*args, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status gated_rmsnorm(const void* x, const void* z, const void* weight, void* out,
+                         int64_t rows, int32_t d, int32_t group_size, float eps, ssd_dtype act,
+                         ssd_dtype wt, ssd_stream_t stream) {
+  if (!weight || rows < 0 || d < 1 || group_size < 1 || d % group_size != 0)
+    return SSD_ERR_INVALID_ARG;
+  if (rows > 0 && (!x || !out)) return SSD_ERR_INVALID_ARG;
+  if (bad_dtype(act) || bad_dtype(wt) || !(eps >= 0.f)) return SSD_ERR_INVALID_ARG;
+  if ((rows * (int64_t)(d / group_size) + 7) / 8 > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_gated_rmsnorm(x, z, weight, out, rows, d, group_size, eps, act, wt, st) ==
+                 cudaSuccess
+             ? SSD_OK
+             : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_read_status(uint32_t* d_status, int32_t clear, uint32_t* bits_out,
+                           ssd_stream_t stream) {
+  if (!d_status) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, d_status, sizeof(bits), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  if (clear && cudaMemsetAsync(d_status, 0, sizeof(uint32_t), st) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  if (bits & SSD_DEV_A_NOT_NEG) return SSD_ERR_A_NOT_NEGATIVE;
+  if (bits & SSD_DEV_INDEX_OOR) return SSD_ERR_INDEX;
+  if (bits & SSD_DEV_SEQ_META) return SSD_ERR_SEQ_META;
+  if (bits & SSD_DEV_TIMEOUT) return SSD_ERR_TIMEOUT;
+  return SSD_OK;
+}
+
+const char* ssd_status_string(ssd_status s) {
+  switch (s) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED";
+    case SSD_ERR_A_NOT_NEGATIVE: return "SSD_ERR_A_NOT_NEGATIVE";
+    case SSD_ERR_INDEX: return "SSD_ERR_INDEX";
+    case SSD_ERR_SEQ_META: return "SSD_ERR_SEQ_META";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT";
+  }
+  return "SSD_ERR_UNKNOWN";
+}
+
+int32_t ssd_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// ssd_internal.cuh -- declarations shared by the translation units of libssd.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// Activation load/store in fp32 registers.
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// dt preprocessing: softplus(raw + bias) (log1p(e^v), identity above 20) or the plain sum.
+__device__ __forceinline__ float dt_prep(float raw, float bias, int softplus) {
+  float v = raw + bias;
+  if (!softplus) return v;
+  return v > 20.f ? v : log1pf(expf(v));
+}
+
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t bit) {
+  if (st) atomicOr(st, bit);
+}
+
+// Launchers (each returns cudaSuccess or the launch error).
+cudaError_t launch_state_update(const ssd_update_args& a, cudaStream_t s);
+cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, void* out,
+                                 int64_t rows, int d, int gs, float eps, ssd_dtype act,
+                                 ssd_dtype wt, cudaStream_t s);
+cudaError_t launch_scan_simt(const ssd_scan_args& a, cudaStream_t s);
+
+// Tensor-core scan: returns SSD_ERR_UNSUPPORTED for shapes it cannot take.
+bool scan_tc_supported(const ssd_scan_args& a, int* p_block_out);
+ssd_status launch_scan_tc(const ssd_scan_args& a, int p_block, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,110 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports every entry
+point include/ssd.h declares, its argument structs have the C layout the binding
+assumes, and host-side validation rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from mamba2_ssd_state_gb300 import build as B
+from mamba2_ssd_state_gb300 import ssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ssd.load_library()
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = ssd.header_functions()
+    assert set(names) == {"ssd_chunk_scan", "ssd_state_update", "gated_rmsnorm",
+                          "ssd_read_status", "ssd_status_string", "ssd_version"}
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+    # nothing but the C ABI is exported
+    assert exported == set(names)
+
+
+def test_struct_layout_matches_c(tmp_path):
+    fields = {"ssd_scan_args": ssd.ScanArgs, "ssd_update_args": ssd.UpdateArgs}
+    src = ["#include <stdio.h>", "#include <stddef.h>", '#include "ssd.h"', "int main(void){"]
+    for cname, cls in fields.items():
+        src.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            src.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    src.append("return 0;}")
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", f"-I{ROOT}/include", str(c), "-o", str(exe)], check=True)
+    got = dict(ln.rsplit(" ", 1) for ln in subprocess.run([str(exe)], capture_output=True,
+                                                          text=True, check=True).stdout.split("\n") if ln)
+    for cname, cls in fields.items():
+        assert int(got[cname]) == ctypes.sizeof(cls)
+        for f, _ in cls._fields_:
+            assert int(got[f"{cname}.{f}"]) == getattr(cls, f).offset, f
+
+
+def _scan_args(**kw):
+    a = ssd.ScanArgs()
+    a.struct_size = ctypes.sizeof(ssd.ScanArgs)
+    a.x = a.dt = a.A = a.B = a.C = a.cu_seqlens = a.y = 0x1000
+    a.nseq, a.T, a.H, a.P, a.G, a.N, a.chunk_size = 1, 8, 4, 16, 2, 16, 16
+    a.act_dtype = ssd.SSD_F32
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(struct_size=8), dict(A=None), dict(cu_seqlens=None), dict(x=None), dict(nseq=0),
+    dict(H=3), dict(G=0), dict(P=0), dict(N=0), dict(chunk_size=0), dict(chunk_size=257),
+    dict(act_dtype=7), dict(x_stride_t=10), dict(B_stride_t=5), dict(impl=9), dict(p_block=48),
+])
+def test_scan_rejects_bad_arguments(lib, bad):
+    a = _scan_args(**bad)
+    assert lib.ssd_chunk_scan(ctypes.byref(a), None) == 1
+    assert lib.ssd_chunk_scan(None, None) == 1
+
+
+def test_update_rejects_bad_arguments(lib):
+    a = ssd.UpdateArgs()
+    a.struct_size = ctypes.sizeof(ssd.UpdateArgs)
+    assert lib.ssd_state_update(ctypes.byref(a), None) == 1          # NULL pool
+    a.state_pool = a.A = a.state_indices = a.x = a.dt = a.B = a.C = a.y = 0x1000
+    a.num_slots, a.batch, a.H, a.P, a.G, a.N = 4, 2, 4, 16, 3, 16    # H % G != 0
+    assert lib.ssd_state_update(ctypes.byref(a), None) == 1
+    a.G = 2
+    a.slot_stride = 5                                                 # smaller than a slot
+    assert lib.ssd_state_update(ctypes.byref(a), None) == 1
+    a.slot_stride, a.batch = 0, 70000                                 # beyond the grid limit
+    assert lib.ssd_state_update(ctypes.byref(a), None) == 2
+
+
+def test_norm_rejects_bad_arguments(lib):
+    p = 0x1000
+    assert lib.gated_rmsnorm(p, p, p, p, 4, 64, 48, 1e-5, 1, 1, None) == 1   # 64 % 48
+    assert lib.gated_rmsnorm(p, p, None, p, 4, 64, 64, 1e-5, 1, 1, None) == 1
+    assert lib.gated_rmsnorm(p, p, p, p, 4, 64, 64, -1.0, 1, 1, None) == 1
+    assert lib.gated_rmsnorm(p, p, p, p, 4, 64, 64, 1e-5, 3, 1, None) == 1
+    assert lib.ssd_read_status(None, 1, None, None) == 1
+
+
+def test_status_strings_and_version(lib):
+    assert lib.ssd_status_string(0) == b"SSD_OK"
+    assert lib.ssd_status_string(3) == b"SSD_ERR_A_NOT_NEGATIVE"
+    assert lib.ssd_version() >= 100
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(ssd, "_lib", None)
+    with pytest.raises(RuntimeError):
+        ssd.load_library(str(tmp_path / "nope.so"))

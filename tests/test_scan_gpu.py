@@ -1,0 +1,175 @@
+"""GPU parity of ssd_chunk_scan against the double-precision oracle.
+
+fp32 inputs are held to rtol(K) (tolerance.py); bf16 inputs to rel-L2 <= 1e-2 and
+max-abs <= 5e-2 on y and on the final states.  Shapes span several 128-token tiles,
+ragged tails, one-token and empty sequences, and the full workload sizes (the large one
+checked on a sample of heads computed by the oracle).
+"""
+import numpy as np
+import pytest
+import torch
+
+from mamba2_ssd_state_gb300 import inputs as I
+from mamba2_ssd_state_gb300 import ssd
+from gpu_util import dev, scan_gpu, scan_oracle
+from tolerance import check_bf16, check_fp32, scan_K
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_fp32_scan(name, s, y, fs):
+    yr, fr, ya, fa = scan_oracle(s, with_abs=True)
+    Ky, Kf = scan_K(s.cu_seqlens, s.H, s.P, s.N, s.has_initial_state)
+    check_fp32(f"{name} y", y, yr, ya, Ky)
+    check_fp32(f"{name} final", fs, fr, fa, Kf)
+
+
+def test_tiny_fp32_layer():
+    """64 tokens, H=4, P=16, G=1, N=16, chunk 16, fp32, zero initial state."""
+    s = I.scan_workload("tiny_fp32")
+    y, fs, bits = scan_gpu(s)
+    assert bits == 0
+    _check_fp32_scan("tiny_fp32", s, y, fs)
+
+
+@pytest.mark.parametrize("N", [16, 48, 128])
+def test_fp32_varlen_edges(N):
+    s = I.make_scan_inputs([37, 1, 0, 16, 65, 3], H=4, P=16, G=2, N=N, chunk_size=16,
+                           act="f32", seed=101, init=[1, 0, 1, 1, 0, 1])
+    y, fs, bits = scan_gpu(s)
+    assert bits == 0
+    _check_fp32_scan(f"fp32 varlen N={N}", s, y, fs)
+    # the empty sequence returns its initial state
+    np.testing.assert_array_equal(fs[2], s.initial_states.values[2])
+
+
+SEQS = [300, 129, 1, 64, 700, 0, 128, 127, 255]
+
+
+@pytest.mark.parametrize("p_block", [16, 32, 64])
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_bf16_tensor_core_parity(p_block, chunk):
+    s = I.make_scan_inputs(SEQS, H=4, P=64, G=2, N=128, chunk_size=chunk, act="bf16",
+                           seed=103, init=[1, 0, 1, 1, 0, 1, 0, 1, 1])
+    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16(f"tc pb={p_block} Q={chunk} y", y, yr)
+    check_bf16(f"tc pb={p_block} Q={chunk} final", fs, fr)
+
+
+def test_bf16_simt_parity():
+    s = I.make_scan_inputs([200, 1, 57], H=4, P=32, G=2, N=128, chunk_size=128, act="bf16",
+                           seed=107, init=[1, 1, 0])
+    y, fs, bits = scan_gpu(s, impl="simt")
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("simt bf16 y", y, yr)
+    check_bf16("simt bf16 final", fs, fr)
+
+
+def test_tc_without_D_and_final_states():
+    s = I.make_scan_inputs([150, 90], H=2, P=32, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=109, init="all")
+    y, fs, bits = scan_gpu(s, impl="tc", final=False, D=False)
+    assert fs is None and bits == 0
+    yr, _ = scan_oracle(s, D=False)
+    check_bf16("tc no-D y", y, yr)
+
+
+def test_tc_strided_projection_layout():
+    """x, B and C read zero-copy as column slices of one packed projection buffer."""
+    Ls, H, P, G, N = [333, 64], 4, 64, 2, 128
+    s = I.make_scan_inputs(Ls, H=H, P=P, G=G, N=N, chunk_size=128, act="bf16", seed=113,
+                           init=[1, 0])
+    T = s.T
+    W = H * P + 2 * G * N + 64          # pad so the token stride is not the dense size
+    buf = torch.zeros((T, W), dtype=torch.bfloat16, device="cuda")
+    buf[:, :H * P] = dev(s.x).view(T, H * P)
+    buf[:, H * P:H * P + G * N] = dev(s.B).view(T, G * N)
+    buf[:, H * P + G * N:H * P + 2 * G * N] = dev(s.C).view(T, G * N)
+    x = buf[:, :H * P].view(T, H, P)
+    B = buf[:, H * P:H * P + G * N].view(T, G, N)
+    C = buf[:, H * P + G * N:H * P + 2 * G * N].view(T, G, N)
+    yr, fr = scan_oracle(s)
+    for impl in ("tc", "simt"):
+        y, fs = ssd.chunk_scan(x, dev(s.dt), dev(s.A), B, C,
+                               cu_seqlens=torch.from_numpy(s.cu_seqlens).cuda(), chunk_size=128,
+                               D=dev(s.D), dt_bias=dev(s.dt_bias),
+                               initial_states=dev(s.initial_states),
+                               has_initial_state=torch.from_numpy(s.has_initial_state).cuda(),
+                               impl=impl)
+        check_bf16(f"strided {impl} y", y.float().cpu().numpy(), yr)
+        check_bf16(f"strided {impl} final", fs.cpu().numpy(), fr)
+
+
+def test_tc_and_simt_agree():
+    s = I.make_scan_inputs([513, 77], H=4, P=64, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=127, init=[1, 1])
+    y1, f1, _ = scan_gpu(s, impl="tc")
+    y2, f2, _ = scan_gpu(s, impl="simt")
+    check_bf16("tc vs simt y", y1, y2)
+    check_bf16("tc vs simt final", f1, f2)
+
+
+@pytest.mark.parametrize("impl", ["tc", "simt"])
+def test_A_not_negative_sets_status(impl):
+    s = I.make_scan_inputs([140], H=3, P=32, G=1, N=128, chunk_size=128, act="bf16", seed=131,
+                           init="all")
+    A = s.A.values.copy()
+    A[1] = 0.0
+    s.A = I.Tensor(A, "f32")
+    y, fs, bits = scan_gpu(s, impl=impl)
+    assert bits & ssd.DEV_A_NOT_NEG
+    assert np.all(y[:, 1] == 0) and np.all(fs[:, 1] == 0)
+    yr, fr = scan_oracle(s, heads=[0, 2])
+    check_bf16(f"{impl} good heads y", y[:, [0, 2]], yr)
+
+
+@pytest.mark.parametrize("impl", ["tc", "simt"])
+def test_bad_cu_seqlens_sets_status(impl):
+    s = I.make_scan_inputs([100, 50], H=2, P=32, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=137)
+    cu = torch.tensor([0, 120, 100], dtype=torch.int32, device="cuda")  # decreasing
+    status = ssd.new_status()
+    ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C), cu_seqlens=cu,
+                   chunk_size=128, status=status, impl=impl)
+    rc, bits = ssd.read_status(status)
+    assert bits & ssd.DEV_SEQ_META
+    assert rc == 5
+
+
+def test_host_validation_errors():
+    s = I.make_scan_inputs([16], H=2, P=16, G=1, N=16, chunk_size=16, act="f32", seed=139)
+    cu = torch.from_numpy(s.cu_seqlens).cuda()
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C), cu_seqlens=cu,
+                       chunk_size=0)
+    assert e.value.code == 1
+    with pytest.raises(ssd.SsdError) as e:   # fp32 has no tensor-core path
+        ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C), cu_seqlens=cu,
+                       chunk_size=16, impl="tc")
+    assert e.value.code == 2
+
+
+# ----------------------------------------------------------------------------- full sizes
+
+def test_mamba2_130m_layer_full():
+    """2 x 2048 tokens, H=24, P=64, G=1, N=128, chunk 256, initial states: whole output."""
+    s = I.scan_workload("mamba2_130m")
+    y, fs, bits = scan_gpu(s)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("mamba2_130m y", y, yr)
+    check_bf16("mamba2_130m final", fs, fr)
+
+
+def test_nemotron_h_varlen_sampled_heads():
+    """4 packed sequences (8192, 3000, 517, 4675), H=128, G=8: heads from every group."""
+    s = I.scan_workload("nemotron_h_varlen")
+    y, fs, bits = scan_gpu(s)
+    assert bits == 0
+    heads = [0, 17, 38, 63, 64, 90, 111, 127]
+    yr, fr = scan_oracle(s, heads=heads)
+    check_bf16("nemotron_h sampled y", y[:, heads], yr)
+    check_bf16("nemotron_h sampled final", fs[:, heads], fr)

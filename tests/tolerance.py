@@ -1,0 +1,65 @@
+"""Comparison bars for the GPU path against the double-precision oracle.
+
+fp32 paths use the bar of the vllm.cpp page "W2 finish (KERNEL-SSM-MAMBA)" (section
+"Evidence" and the #675 message): rtol(K) = 4 (K + 2) 2^-24 for an output produced by a
+length-K recurrence / summation, applied here relative to the sum of the magnitudes of
+every term that produced the output (the classical summation-error scale), plus the
+smallest normal fp32 number.  Against an exact reference only the device's own
+rounding counts (<= 2 ulp per expf, (K - 1) u summation).
+
+bf16-input paths use relative L2 <= 1e-2 and max-abs <= 5e-2 per tensor.
+
+Every comparison prints the fraction of its bar used, so a bar that stopped doing work
+would show.
+"""
+import numpy as np
+
+U = 2.0 ** -24
+TINY = 2.0 ** -126
+
+
+def rtol_K(K):
+    return 4.0 * (np.asarray(K, dtype=np.float64) + 2.0) * U
+
+
+def check_fp32(name, got, ref, scale, K):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bar = rtol_K(K) * np.asarray(scale, dtype=np.float64) + TINY
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    frac = float(np.max(err / bar)) if err.size else 0.0
+    print(f"[bar] {name}: fp32 worst element used {100 * frac:.3f}% of rtol(K)")
+    assert frac <= 1.0, f"{name}: error exceeds rtol(K) by {frac:.3f}x"
+    return frac
+
+
+def check_bf16(name, got, ref, rel_l2_max=1e-2, max_abs_max=5e-2):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    if ref.size == 0:
+        return 0.0, 0.0
+    rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    mx = float(np.max(np.abs(got - ref)))
+    print(f"[bar] {name}: rel-L2 {rel:.3e} ({100 * rel / rel_l2_max:.1f}% of bar), "
+          f"max-abs {mx:.3e} ({100 * mx / max_abs_max:.1f}% of bar)")
+    assert rel <= rel_l2_max, f"{name}: rel-L2 {rel:.3e} > {rel_l2_max}"
+    assert mx <= max_abs_max, f"{name}: max-abs {mx:.3e} > {max_abs_max}"
+    return rel, mx
+
+
+def scan_K(cu_seqlens, H, P, N, has_init):
+    """K of every y[t,h,p] (tokens since the sequence start, + 1 with an initial state,
+    + N) and of every final state entry (sequence length + 1)."""
+    cu = np.asarray(cu_seqlens)
+    T = int(cu[-1])
+    Ky = np.zeros((T, 1, 1))
+    nseq = len(cu) - 1
+    Kf = np.zeros((nseq, 1, 1, 1))
+    for s in range(nseq):
+        a, b = int(cu[s]), int(cu[s + 1])
+        init = 1 if (has_init is not None and has_init[s]) else 0
+        Ky[a:b, 0, 0] = np.arange(1, b - a + 1) + init + N
+        Kf[s] = (b - a) + 1
+    return Ky, Kf
