@@ -183,6 +183,14 @@ def run_ours(args, rank, world, local_rank):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
+    # the timed region is milliseconds long: keep the GPU under the same load for a
+    # second first, so the clock samples (100 ms apart) cover the state it is timed in
+    t_load = time.perf_counter()
+    while time.perf_counter() - t_load < 1.0:
+        for _ in range(50):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -423,6 +431,55 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def profile_only(args):
+    """Launch one op on its benchmark workload warmup + steps times, nothing else."""
+    import torch
+
+    from mamba2_ssd_state_gb300 import build as lib_build
+    from mamba2_ssd_state_gb300 import inputs as I
+    from mamba2_ssd_state_gb300 import ssd
+
+    lib_build.build()
+    dev = torch.device("cuda", 0)
+
+    def T_(t):
+        dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
+        return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
+
+    if args.profile in ("scan", "scan_large", "norm"):
+        name = WORKLOAD if args.profile != "scan_large" else "nemotron_h_varlen"
+        s = I.scan_workload(name)
+        x, dt, A, B, C, Dp, bias, init = (T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D,
+                                                            s.dt_bias, s.initial_states))
+        hi = torch.from_numpy(s.has_initial_state).to(dev)
+        cu = torch.from_numpy(s.cu_seqlens).to(dev)
+        y = torch.empty_like(x)
+        fs = torch.empty((s.nseq, s.H, s.P, s.N), dtype=torch.float32, device=dev)
+        if args.profile == "norm":
+            w = I.WORKLOADS[WORKLOAD]
+            nrm = I.make_norm_inputs(s.T, s.H * s.P, w["norm_group"], act="bf16", seed=w["seed"] + 50)
+            z, wt = T_(nrm.z), T_(nrm.weight)
+            out = torch.empty((s.T, s.H * s.P), dtype=torch.bfloat16, device=dev)
+            run = lambda: ssd.gated_rmsnorm(y.view(s.T, -1), z, wt, group_size=w["norm_group"],  # noqa
+                                            out=out)
+        else:
+            run = lambda: ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size,  # noqa
+                                         D=Dp, dt_bias=bias, initial_states=init,
+                                         has_initial_state=hi, y=y, final_states=fs)
+    else:
+        H, P, G, N, S, batch = 128, 64, 8, 128, 512, 256
+        idx = I.padded_permutation(S, batch, seed=3000 + batch)
+        u = I.make_update_inputs(1, idx, H, P, G, N, act="bf16", seed=3100 + batch,
+                                 pool_values=np.zeros((1, H, P, N), np.float32))
+        pool = torch.randn((S, H, P, N), device=dev, dtype=torch.float32)
+        a = (pool, torch.from_numpy(idx).to(dev), T_(u.x), T_(u.dt), T_(u.A), T_(u.B), T_(u.C))
+        run = lambda: ssd.state_update(*a, D=T_(u.D), dt_bias=T_(u.dt_bias))  # noqa
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    print(f"profile {args.profile}: {args.warmup + args.steps} launches done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,7 +488,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / large-scan legs")
+    ap.add_argument("--profile", choices=["scan", "scan_large", "norm", "update"],
+                    help="only launch this op's benchmark workload steps times (for ncu)")
     args = ap.parse_args()
+    if args.profile:
+        profile_only(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

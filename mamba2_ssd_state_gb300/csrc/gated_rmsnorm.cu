@@ -14,6 +14,13 @@ namespace ssd {
 namespace {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+// bf16 outputs carry 2^-9 relative rounding, far above the fast exponential's and
+// reciprocal's few-ulp error, so the bf16 path uses them; fp32 keeps expf and division.
+__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.f + __expf(-z)); }
+template <typename TA> __device__ __forceinline__ float gate(float z) {
+  if constexpr (sizeof(TA) == 2) return silu_fast(z);
+  else return silu(z);
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -79,7 +86,7 @@ __global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
       float zv[8];
       Vec8<TA>::load(z + base + off, zv);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) g[i][e] = xv[e] * silu(zv[e]);
+      for (int e = 0; e < 8; ++e) g[i][e] = xv[e] * gate<TA>(zv[e]);
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) g[i][e] = xv[e];
@@ -118,14 +125,14 @@ __global__ void __launch_bounds__(256) norm_generic_kernel(const TA* x,
   float ss = 0.f;
   for (int k = lane; k < gs; k += 32) {
     float gv = to_f32(x[base + k]);
-    if (z) gv *= silu(to_f32(z[base + k]));
+    if (z) gv *= gate<TA>(to_f32(z[base + k]));
     ss = fmaf(gv, gv, ss);
   }
   ss = warp_sum(ss);
   const float r = rsqrtf(ss / (float)gs + eps);
   for (int k = lane; k < gs; k += 32) {
     float gv = to_f32(x[base + k]);
-    if (z) gv *= silu(to_f32(z[base + k]));
+    if (z) gv *= gate<TA>(to_f32(z[base + k]));
     out[base + k] = from_f32<TA>(gv * r * to_f32(w[col0 + k]));
   }
 }

@@ -5,28 +5,42 @@
 // states[c-1] feeding chunk c, M4 the D skip) names the parts computed here.  With
 // a_t = dt_t A and, inside a chunk, cs_i = sum_{r<=i} a_r:
 //     CB[i,j]  = C_i . B_j                                   (tensor core, fp32 in TMEM)
-//     M[i,j]   = CB[i,j] exp(cs_i - cs_j) dt_j,  j <= i       (segsum decay, epilogue)
+//     M[i,j]   = CB[i,j] exp(cs_i - cs_j) dt_j,  j <= i       (segsum decay, mask warps)
 //     Y        = M x                                          (tensor core, A from TMEM)
 //     S^T      = B^T (w o x),  w_j = exp(cs_last - cs_j) dt_j (chunk state, tensor core)
 //     Yoff     = C h_{c-1}^T                                  (tensor core)
-//     y_i      = Y_i + exp(cs_i) Yoff_i + D x_i               (epilogue, bf16 out)
+//     y_i      = Y_i + exp(cs_i) Yoff_i + D x_i               (fp32, bf16 out)
 //     h_c      = exp(cs_last) h_{c-1} + S                      (state pass, fp32 registers)
 //
 // One CTA owns one (sequence, head, block of PB channels) chain and walks its chunks in
 // order, so the state never leaves the SM: states[c-1] feeds chunk c in place, and HBM
-// sees only x, B, C, dt in and y (plus the per-sequence initial / final states).  The
-// channel split PB (64, 32 or 16) trades redundant C.B^T work for more chains when a
+// sees only x, B, C, dt in and y out (plus the per-sequence initial / final states).
+// The channel split PB (64, 32 or 16) trades redundant C.B^T work for more chains when a
 // workload has few (sequence, head) pairs.
 //
-// Warp roles (320 threads):
-//   warp 0    TMA producer: C, B (two 64-wide 128B-swizzled boxes each) and x per chunk
-//             into a 2-stage ring guarded by full/empty mbarriers.
-//   warp 1    TMEM owner (512 columns) and the single MMA-issuing thread.
-//   warps 2-9 epilogue: two warps per TMEM lane quadrant, each taking half of the
-//             columns.  dt/softplus/cumsum, the decay mask (CB -> M written back to
-//             TMEM as bf16), w o x into shared memory, y, and the fp32 state h.
-// Every wait is bounded; a wait that runs out raises a CTA-wide abort flag, every role
-// then drains what it has in flight and the kernel returns with SSD_DEV_TIMEOUT set.
+// Warp roles (480 threads), pipelined across chunks:
+//   warp 0      TMA producer (one lane): C and B of a chunk (two 64-wide 128B-swizzled
+//               boxes each) into a 2-deep ring freed by the tensor core, x into a ring
+//               freed by the mask and output warps, plus L2 prefetches further ahead.
+//   warp 1      TMEM owner (512 columns); one lane issues every MMA, in whatever order
+//               their inputs become ready.
+//   warps 2-9   mask warps (two per TMEM lane quadrant): C.B^T -> M (bf16, written
+//               back to TMEM as the A operand of Y = M x) and w o x into shared memory.
+//   warps 10-13 output warps (one per quadrant): first the state, h = 2^cs_last h + S
+//               in fp32 registers and h^T (bf16) for the next chunk's Yoff, then
+//               y = Y + 2^cs_i Yoff + D x, then the final state.
+//   warp 14     decay warp: dt (softplus), the base-2 cumulative decay, the column
+//               factors of the mask and the chunk-state weights w, chunks ahead.
+// TMEM: C.B^T (128 columns), M (64), Y x2, S, Yoff x2 (PB each).  Y, Yoff and h^T are
+// double-buffered, so chunk c+1's products run while chunk c's outputs are read; the
+// state chain per chunk is S -> h -> h^T -> Yoff of the next chunk.  Every wait is
+// bounded; a wait that runs out raises a CTA-wide abort flag, every role then drains
+// what it has in flight and the kernel returns with SSD_DEV_TIMEOUT set.
+//
+// Decay mask arithmetic: exp(cs_i - cs_j) = 2^(cs2_i - cs2_a) * 2^(cs2_a - cs2_j) with the
+// anchor a the first token of j's 32-column block, so the mask costs two multiplies
+// per element instead of an exponential.  The decay warp checks, per block, that both
+// factors stay at most 2^64; a block that fails takes the exact per-element exponential.
 //
 // The chunk is the 128-row tcgen05 tile: sequences are split into 128-token chunks
 // starting at their first token.  Chunked evaluation is exact for any chunk length, so
@@ -45,15 +59,31 @@ using namespace tc;
 
 constexpr int QT = 128;          // chunk length = tcgen05 M
 constexpr int NSTATE = 128;      // state size N of this kernel
-constexpr int NST = 2;           // TMA ring depth
-constexpr int kThreads = 320;
+constexpr int NBC = 2;           // TMA ring depth of B and C
+constexpr int NB = 3;            // depth of the decay buffer ring
+constexpr int kMaskWarps = 8, kOutWarps = 4;
+constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
+constexpr int kThreads = 32 * (kDecayWarp + 1);
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kFactorLimit = 64.f;            // log2 bound of a factorised decay factor
 constexpr long long kWaitLimit = 4000000000LL;  // SM cycles (about 2 s)
 
-// TMEM columns
-constexpr uint32_t kColCB = 0;    // two fp32 128x128 C.B^T buffers: [0,128) and [128,256)
-constexpr uint32_t kColM = 256;   // bf16 decay-masked M, 64 columns (two values per column)
-constexpr uint32_t kColY = 320;   // Y, then Yoff, then S, PB columns each
+// TMEM columns (fp32 unless noted)
+constexpr uint32_t kColCB = 0;    // C.B^T, 128 columns
+constexpr uint32_t kColM = 128;   // bf16 decay-masked M, 64 columns (two values per column)
+constexpr uint32_t kColAcc = 192; // Y[2], S, Yoff[2]: PB columns each (5 PB <= 320)
+
+// decay buffer: per chunk, float arrays of QT
+constexpr int kProCs = 0, kProDt = QT, kProColf = 2 * QT, kProW = 3 * QT, kProSafe = 4 * QT;
+constexpr int kProStride = 4 * QT + 8;  // floats
+
+#ifdef SSD_TRACE
+__device__ long long g_trace[64][16];
+#define TRACE(c, slot) \
+  do { if (blockIdx.x == 0 && (c) < 64) g_trace[(c)][(slot)] = clock64(); } while (0)
+#else
+#define TRACE(c, slot) do { } while (0)
+#endif
 
 struct TcParams {
   const float* dt;
@@ -71,34 +101,43 @@ struct TcParams {
 
 template <int PB>
 struct Layout {
+  static constexpr int NX = PB == 64 ? 2 : 3;          // TMA ring depth of x
   static constexpr int kXRow = PB * 2;                 // bytes per token row of x / x' / h^T
   static constexpr int kXBytes = QT * kXRow;
   static constexpr int kXPad = (kXBytes + 1023) / 1024 * 1024;
-  static constexpr int kStageC = 0;                    // C: two [128 x 64] bf16 boxes
-  static constexpr int kStageB = 32768;                // B: two boxes
-  static constexpr int kStageX = 65536;                // x: one [128 x PB] box
-  static constexpr int kStage = 65536 + kXPad;
-  static constexpr int kXs = NST * kStage;             // w o x
-  static constexpr int kHT = kXs + kXPad;              // h^T, [N rows][PB] bf16
+  static constexpr int kBC = 0;                        // NBC x (C: 32 KB, B: 32 KB)
+  static constexpr int kBCStage = 65536;
+  static constexpr int kX = NBC * kBCStage;            // NX x x tile
+  static constexpr int kXs = kX + NX * kXPad;          // w o x
+  static constexpr int kHT = kXs + kXPad;              // h^T x 2, [N rows][PB] bf16 each
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
-  static constexpr int kDt = kHT + kHTPad;             // float [2][QT]
-  static constexpr int kCs = kDt + 2 * QT * 4;         // float [2][QT] (base-2 cumsum)
-  static constexpr int kBar = kCs + 2 * QT * 4;        // mbarriers
-  static constexpr int kNumBar = 2 * NST + 4 + 4 + 6;
+  static constexpr int kPro = kHT + 2 * kHTPad;        // float [NB][kProStride]
+  static constexpr int kBar = kPro + NB * kProStride * 4;
+  static constexpr int kNumBar = 2 * NBC + 2 * NX + 2 * NB + 12;
   static constexpr int kFlags = kBar + kNumBar * 8;    // abort flag, TMEM base
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
   static constexpr int kSwB = PB == 64 ? 3 : PB == 32 ? 2 : 1;  // Swizzle<B,4,3>
   static constexpr uint32_t kSwCode = PB == 64 ? kSw128 : PB == 32 ? kSw64 : kSw32;
-  static constexpr uint32_t kTxBytes = 65536 + kXBytes;
+  // accumulator columns
+  static constexpr uint32_t kY0 = kColAcc, kS = kColAcc + 2 * PB, kO0 = kColAcc + 3 * PB;
 };
+
+// softplus for the bf16 path: exp(v) alone below -8 (log1p(e) = e (1 - e/2 ...), relative
+// error < 2e-4 there), else log(1 + e^v) with the fast exponential and logarithm; the
+// error stays far below bf16's 2^-9.
+__device__ __forceinline__ float softplus_fast(float v) {
+  if (v > 20.f) return v;
+  const float e = __expf(v);
+  return v < -8.f ? e : __logf(1.f + e);
+}
 
 template <int PB>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams prm) {
   using L = Layout<PB>;
-  constexpr int PH = PB / 2;  // columns per epilogue half
+  constexpr int NX = L::NX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
@@ -131,40 +170,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nch = (t1 - t0 + QT - 1) / QT;
 
-  float* dt_s = reinterpret_cast<float*>(sm + L::kDt);
-  float* cs_s = reinterpret_cast<float*>(sm + L::kCs);
+  float* pro = reinterpret_cast<float*>(sm + L::kPro);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
-  uint64_t* full = bars;                 // [NST]  TMA landed
-  uint64_t* empty = bars + NST;          // [NST]  stage free (MMA commit + 8 epilogue warps)
-  uint64_t* cb_full = bars + 2 * NST;    // [2]    C.B^T ready in TMEM
-  uint64_t* cb_empty = cb_full + 2;      // [2]    C.B^T consumed (8 warps)
-  uint64_t* pro_full = cb_empty + 2;     // [2]    dt / cumsum of a chunk in smem (4 warps)
-  uint64_t* pro_empty = pro_full + 2;    // [2]    dt / cumsum buffer consumed (8 warps)
-  uint64_t* m_ready = pro_empty + 2;     //        M in TMEM and w o x in smem (8 warps)
-  uint64_t* acc_full = m_ready + 1;      //        Y and S done
-  uint64_t* yoff_full = m_ready + 2;     //        Yoff done
-  uint64_t* acc_empty = m_ready + 3;     //        Y, Yoff, S read (8 warps)
-  uint64_t* h_ready = m_ready + 4;       //        h^T in smem (8 warps)
-  uint64_t* drain = m_ready + 5;         //        teardown: all MMAs retired
+  uint64_t* bc_full = bars;                 // [NBC] B, C landed
+  uint64_t* bc_empty = bc_full + NBC;       // [NBC] B, C free (MMA commit after Yoff)
+  uint64_t* x_full = bc_empty + NBC;        // [NX]  x landed
+  uint64_t* x_empty = x_full + NX;          // [NX]  x free (8 mask + 4 output warps)
+  uint64_t* pro_full = x_empty + NX;        // [NB]  decay of a chunk ready (decay warp)
+  uint64_t* pro_empty = pro_full + NB;      // [NB]  consumed (8 mask + 4 output warps)
+  // Single barriers track one phase per chunk; a resource with two buffers gets one
+  // barrier per buffer, so no waiter can fall two phases behind its barrier.
+  uint64_t* cb_full = pro_empty + NB;       //       C.B^T in TMEM
+  uint64_t* cb_empty = cb_full + 1;         //       C.B^T read (8 mask warps)
+  uint64_t* m_ready = cb_full + 2;          //       M in TMEM, w o x in smem (8 mask warps)
+  uint64_t* ys_full = cb_full + 3;          //       Y and S done (frees M and w o x)
+  uint64_t* s_empty = cb_full + 4;          //       S read (4 output warps)
+  uint64_t* h_ready = cb_full + 5;          // [2]   h^T buffer written (4 output warps)
+  uint64_t* yoff_full = cb_full + 7;        // [2]   Yoff buffer done
+  uint64_t* y_empty = cb_full + 9;          // [2]   Y and Yoff buffers read (4 output warps)
+  uint64_t* drain = cb_full + 11;           //       teardown: all MMAs retired
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + 8);
+    for (int i = 0; i < NBC; ++i) {
+      mbar_init(&bc_full[i], 1);
+      mbar_init(&bc_empty[i], 1);
     }
+    for (int i = 0; i < NX; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], kMaskWarps + kOutWarps);
+    }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&pro_full[i], 1);
+      mbar_init(&pro_empty[i], kMaskWarps + kOutWarps);
+    }
+    mbar_init(cb_full, 1);
+    mbar_init(cb_empty, kMaskWarps);
+    mbar_init(m_ready, kMaskWarps);
+    mbar_init(ys_full, 1);
+    mbar_init(s_empty, kOutWarps);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&cb_full[i], 1);
-      mbar_init(&cb_empty[i], 8);
-      mbar_init(&pro_full[i], 4);
-      mbar_init(&pro_empty[i], 8);
+      mbar_init(&h_ready[i], kOutWarps);
+      mbar_init(&yoff_full[i], 1);
+      mbar_init(&y_empty[i], kOutWarps);
     }
-    mbar_init(m_ready, 8);
-    mbar_init(acc_full, 1);
-    mbar_init(yoff_full, 1);
-    mbar_init(acc_empty, 8);
-    mbar_init(h_ready, 8);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -182,284 +232,401 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
+    return warp_wait(bar, par, abort_flag, kWaitLimit);
+  };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (lane 0)
     if (lane == 0) {
-      int issued = 0;
-      for (int c = 0; c < nch; ++c) {
-        const int st = c % NST;
-        if (c >= NST && !mbar_wait(&empty[st], ((c / NST) - 1) & 1, abort_flag, kWaitLimit))
-          break;
-        uint8_t* stg = sm + st * L::kStage;
+      constexpr int kAhead = 2;  // L2 prefetch distance beyond the rings, in chunks
+      for (int c = 0; c < NBC + kAhead && c < nch; ++c) {
         const int tok = t0 + c * QT;
-        mbar_arrive_expect_tx(&full[st], L::kTxBytes);
-        tma_load_3d(stg + L::kStageC, &tmC, &full[st], 0, g, tok);
-        tma_load_3d(stg + L::kStageC + 16384, &tmC, &full[st], 64, g, tok);
-        tma_load_3d(stg + L::kStageB, &tmB, &full[st], 0, g, tok);
-        tma_load_3d(stg + L::kStageB + 16384, &tmB, &full[st], 64, g, tok);
-        tma_load_3d(stg + L::kStageX, &tmX, &full[st], p0, h, tok);
-        issued = c + 1;
+        tma_prefetch_3d(&tmC, 0, g, tok);
+        tma_prefetch_3d(&tmC, 64, g, tok);
+        tma_prefetch_3d(&tmB, 0, g, tok);
+        tma_prefetch_3d(&tmB, 64, g, tok);
+        tma_prefetch_3d(&tmX, p0, h, tok);
+      }
+      int bc_issued = 0, x_issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int tok = t0 + c * QT;
+        const int sb = c % NBC, sx = c % NX;
+        if (c >= NBC && !mbar_wait(&bc_empty[sb], ((c / NBC) - 1) & 1, abort_flag, kWaitLimit))
+          break;
+        uint8_t* bc = sm + L::kBC + sb * L::kBCStage;
+        mbar_arrive_expect_tx(&bc_full[sb], 65536);
+        tma_load_3d(bc, &tmC, &bc_full[sb], 0, g, tok);
+        tma_load_3d(bc + 16384, &tmC, &bc_full[sb], 64, g, tok);
+        tma_load_3d(bc + 32768, &tmB, &bc_full[sb], 0, g, tok);
+        tma_load_3d(bc + 49152, &tmB, &bc_full[sb], 64, g, tok);
+        bc_issued = c + 1;
+        if (c + NBC + kAhead < nch) {
+          const int tp = tok + (NBC + kAhead) * QT;
+          tma_prefetch_3d(&tmC, 0, g, tp);
+          tma_prefetch_3d(&tmC, 64, g, tp);
+          tma_prefetch_3d(&tmB, 0, g, tp);
+          tma_prefetch_3d(&tmB, 64, g, tp);
+          tma_prefetch_3d(&tmX, p0, h, tp);
+        }
+        if (c >= NX && !mbar_wait(&x_empty[sx], ((c / NX) - 1) & 1, abort_flag, kWaitLimit))
+          break;
+        mbar_arrive_expect_tx(&x_full[sx], L::kXBytes);
+        tma_load_3d(sm + L::kX + sx * L::kXPad, &tmX, &x_full[sx], p0, h, tok);
+        x_issued = c + 1;
+        TRACE(c, 0);
       }
       // every copy issued must have landed before the CTA's shared memory is released
-      for (int c = issued > NST ? issued - NST : 0; c < issued; ++c)
-        mbar_wait_drain(&full[c % NST], (c / NST) & 1, kWaitLimit);
+      for (int c = bc_issued > NBC ? bc_issued - NBC : 0; c < bc_issued; ++c)
+        mbar_wait_drain(&bc_full[c % NBC], (c / NBC) & 1, kWaitLimit);
+      for (int c = x_issued > NX ? x_issued - NX : 0; c < x_issued; ++c)
+        mbar_wait_drain(&x_full[c % NX], (c / NX) & 1, kWaitLimit);
+    }
+  } else if (warp == kDecayWarp) {
+    // ------------------------------------------------------------ decay warp
+    const float bias = prm.dt_bias ? prm.dt_bias[h] : 0.f;
+    const float a2 = Ah * kLog2e;
+    float dt_raw[4];
+    auto load_dt = [&](int c) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int tok = t0 + c * QT + 32 * k + lane;
+        dt_raw[k] = tok < t1 ? prm.dt[(size_t)tok * H + h] : 0.f;
+      }
+    };
+    if (nch > 0) load_dt(0);
+    for (int c = 0; c < nch; ++c) {
+      const int b = c % NB;
+      if (c >= NB && !wwait(&pro_empty[b], ((c / NB) - 1) & 1)) break;
+      TRACE(c, 1);
+      // dt, base-2 decay a = dt A log2(e), inclusive cumulative sum over the 128 tokens
+      float d[4], cs[4], carry = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int tok = t0 + c * QT + 32 * k + lane;
+        const float v0 = dt_raw[k] + bias;
+        d[k] = tok < t1 ? (prm.dt_softplus ? softplus_fast(v0) : v0) : 0.f;
+        float v = d[k] * a2;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float nb = __shfl_up_sync(0xffffffffu, v, off);
+          if (lane >= off) v += nb;
+        }
+        cs[k] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (c + 1 < nch) load_dt(c + 1);
+      const float cs_last = carry;
+      float* pb = pro + b * kProStride;
+      float run_max = -INFINITY;  // max of cs over blocks >= k (row-factor bound)
+      float blk_max[4];
+#pragma unroll
+      for (int k = 3; k >= 0; --k) {
+        float m = cs[k];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        run_max = fmaxf(run_max, m);
+        blk_max[k] = run_max;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = 32 * k + lane;
+        const float anchor = __shfl_sync(0xffffffffu, cs[k], 0);
+        float span = anchor - cs[k];  // column factor exponent
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, off));
+        pb[kProCs + j] = cs[k];
+        pb[kProDt + j] = d[k];
+        pb[kProColf + j] = ex2(anchor - cs[k]) * d[k];
+        pb[kProW + j] = ex2(cs_last - cs[k]) * d[k];
+        if (lane == 0)
+          pb[kProSafe + k] = (span <= kFactorLimit && blk_max[k] - anchor <= kFactorLimit) ? 1.f : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pro_full[b]);
+      TRACE(c, 2);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (lane 0)
     if (lane == 0) {
       constexpr uint32_t idCB = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idY = make_idesc_bf16(128, PB, false, true);
       constexpr uint32_t idS = make_idesc_bf16(128, PB, true, true);
       constexpr uint32_t idO = make_idesc_bf16(128, PB, false, true);
-      const uint32_t colY = tmem + kColY, colO = tmem + kColY + PB, colS = tmem + kColY + 2 * PB;
-      const uint32_t sXs = smem_u32(sm + L::kXs), sHT = smem_u32(sm + L::kHT);
-      bool ok = true;
-      auto issue_cb = [&](int c) -> bool {
-        const int st = c % NST, cb = c & 1;
-        if (!mbar_wait(&full[st], (c / NST) & 1, abort_flag, kWaitLimit)) return false;
-        if (c >= 2 && !mbar_wait(&cb_empty[cb], ((c >> 1) - 1) & 1, abort_flag, kWaitLimit))
-          return false;
-        tc_fence_after();
-        const uint32_t sC = smem_u32(sm + st * L::kStage + L::kStageC);
-        const uint32_t sB = smem_u32(sm + st * L::kStage + L::kStageB);
+      const uint32_t sXs = smem_u32(sm + L::kXs);
+      // Issue whichever product is ready, each kind in chunk order:
+      //   CB(k)    B, C of k landed; C.B^T of k-1 read by the mask warps
+      //   Y,S(k)   M and w o x of k; Y buffer of k-2 and S of k-1 read
+      //   Yoff(k)  Y,S(k) issued; h^T = h_{k-1}; Yoff buffer of k-2 read
+      int ncb = 0, nys = 0, nyo = 0;
+      long long t_idle = 0;
+      while (nyo < nch) {
+        bool progress = false;
+        if (ncb < nch && mbar_test_wait(&bc_full[ncb % NBC], (ncb / NBC) & 1) &&
+            (ncb == 0 || mbar_test_wait(cb_empty, (ncb - 1) & 1))) {
+          tc_fence_after();
+          const uint32_t sC = smem_u32(sm + L::kBC + (ncb % NBC) * L::kBCStage);
+          const uint32_t sB = sC + 32768;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // K = N = 128 in steps of 16 (32 bytes)
-          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + kColCB + cb * 128, make_sdesc(sC + ko, 16, 1024, kSw128),
-                 make_sdesc(sB + ko, 16, 1024, kSw128), idCB, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {  // K = N = 128 in steps of 16 (32 bytes)
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tmem + kColCB, make_sdesc(sC + ko, 16, 1024, kSw128),
+                   make_sdesc(sB + ko, 16, 1024, kSw128), idCB, kk > 0);
+          }
+          mma_commit(cb_full);
+          ++ncb;
+          progress = true;
         }
-        mma_commit(&cb_full[cb]);
-        return true;
-      };
-      if (nch > 0) ok = issue_cb(0);
-      for (int c = 0; ok && c < nch; ++c) {
-        const int st = c % NST;
-        if (c + 1 < nch && !(ok = issue_cb(c + 1))) break;
-        if (!(ok = mbar_wait(m_ready, c & 1, abort_flag, kWaitLimit))) break;
-        if (c >= 1 && !(ok = mbar_wait(acc_empty, (c - 1) & 1, abort_flag, kWaitLimit))) break;
-        tc_fence_after();
-        const uint32_t sX = smem_u32(sm + st * L::kStage + L::kStageX);
-        const uint32_t sB = smem_u32(sm + st * L::kStage + L::kStageB);
-        const uint32_t sC = smem_u32(sm + st * L::kStage + L::kStageC);
+        if (nys < ncb && mbar_test_wait(m_ready, nys & 1) &&
+            mbar_test_wait(&x_full[nys % NX], (nys / NX) & 1) &&
+            (nys < 1 || mbar_test_wait(s_empty, (nys - 1) & 1)) &&
+            (nys < 2 || mbar_test_wait(&y_empty[nys & 1], ((nys >> 1) - 1) & 1))) {
+          tc_fence_after();
+          TRACE(nys, 3);
+          const uint32_t sX = smem_u32(sm + L::kX + (nys % NX) * L::kXPad);
+          const uint32_t sB = smem_u32(sm + L::kBC + (nys % NBC) * L::kBCStage) + 32768;
+          const uint32_t colY = tmem + L::kY0 + (nys & 1) * PB;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // Y = M x : K = 128 tokens, M from TMEM (8 cols/step)
-          mma_ts(colY, tmem + kColM + kk * 8,
-                 make_sdesc(sX + kk * 16 * L::kXRow, L::kXBytes, 8 * L::kXRow, L::kSwCode), idY,
-                 kk > 0);
+          for (int kk = 0; kk < 8; ++kk)  // Y = M x : K = 128 tokens, M from TMEM (8 cols/step)
+            mma_ts(colY, tmem + kColM + kk * 8,
+                   make_sdesc(sX + kk * 16 * L::kXRow, L::kXBytes, 8 * L::kXRow, L::kSwCode), idY,
+                   kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // S^T = B^T (w o x): A = B read MN-major
-          mma_ss(colS, make_sdesc(sB + kk * 2048, 16384, 1024, kSw128),
-                 make_sdesc(sXs + kk * 16 * L::kXRow, L::kXBytes, 8 * L::kXRow, L::kSwCode), idS,
-                 kk > 0);
-        mma_commit(acc_full);
-        if (!(ok = mbar_wait(h_ready, c & 1, abort_flag, kWaitLimit))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // Yoff = C h^T : K = N = 128
-          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(colO, make_sdesc(sC + ko, 16, 1024, kSw128),
-                 make_sdesc(sHT + kk * 16 * L::kXRow, L::kHTPad, 8 * L::kXRow, L::kSwCode), idO,
-                 kk > 0);
+          for (int kk = 0; kk < 8; ++kk)  // S^T = B^T (w o x): A = B read MN-major
+            mma_ss(tmem + L::kS, make_sdesc(sB + kk * 2048, 16384, 1024, kSw128),
+                   make_sdesc(sXs + kk * 16 * L::kXRow, L::kXBytes, 8 * L::kXRow, L::kSwCode),
+                   idS, kk > 0);
+          mma_commit(ys_full);
+          ++nys;
+          progress = true;
         }
-        mma_commit(yoff_full);
-        mma_commit(&empty[st]);
+        // h_j sits in h^T buffer j & 1 as that buffer's ((j + 1) >> 1)-th value
+        if (nyo < nys && mbar_test_wait(&h_ready[(nyo + 1) & 1], (nyo >> 1) & 1) &&
+            (nyo < 2 || mbar_test_wait(&y_empty[nyo & 1], ((nyo >> 1) - 1) & 1))) {
+          tc_fence_after();
+          TRACE(nyo, 4);
+          const uint32_t sC = smem_u32(sm + L::kBC + (nyo % NBC) * L::kBCStage);
+          const uint32_t sHT = smem_u32(sm + L::kHT + ((nyo + 1) & 1) * L::kHTPad);  // h_{k-1}
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // Yoff = C h^T : K = N = 128
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tmem + L::kO0 + (nyo & 1) * PB, make_sdesc(sC + ko, 16, 1024, kSw128),
+                   make_sdesc(sHT + kk * 16 * L::kXRow, L::kHTPad, 8 * L::kXRow, L::kSwCode), idO,
+                   kk > 0);
+          }
+          mma_commit(&yoff_full[nyo & 1]);
+          mma_commit(&bc_empty[nyo % NBC]);
+          ++nyo;
+          progress = true;
+        }
+        if (progress) {
+          t_idle = 0;
+        } else {
+          if (*abort_flag) break;
+          const long long now = clock64();
+          if (t_idle == 0) t_idle = now;
+          else if (now - t_idle > kWaitLimit) {
+            *abort_flag = 1;
+            break;
+          }
+          __nanosleep(20);
+        }
       }
       mma_commit(drain);
       mbar_wait_drain(drain, 0, kWaitLimit);
     }
-  } else {
-    // ------------------------------------------------------------ epilogue (8 warps)
-    const int hf = (warp - 2) >> 2;        // column half
+  } else if (warp < 2 + kMaskWarps) {
+    // ------------------------------------------------------------ mask warps
+    const int hf = (warp - 2) >> 2;        // which two of the four 32-column blocks
     const int q = warp & 3;                // TMEM lane quadrant of this warp
-    const int r = 32 * q + lane;           // token row i (or state row n)
+    const int r = 32 * q + lane;           // token row i (and token row j for w o x)
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
-    const float bias = prm.dt_bias ? prm.dt_bias[h] : 0.f;
-    const float Dh = prm.D ? prm.D[h] : 0.f;
-    const float a2 = Ah * kLog2e;
-    auto ewait = [&](uint64_t* bar, uint32_t par) -> bool {
-      const bool ok = mbar_wait(bar, par, abort_flag, kWaitLimit);
-      return __all_sync(0xffffffffu, ok);
-    };
-    // dt and the base-2 cumulative decay of chunk c, computed by the four hf == 0 warps
-    // (each warp forms the sums of the lower quadrants itself, so no cross-warp step).
-    auto prologue = [&](int c) -> bool {
-      if (hf != 0) return true;
-      const int b = c & 1;
-      if (c >= 2 && !ewait(&pro_empty[b], ((c >> 1) - 1) & 1)) return false;
-      float own_dt = 0.f, own_a = 0.f, pre = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = t0 + c * QT + 32 * k + lane;
-        const float d = tok < t1 ? dt_prep(prm.dt[(size_t)tok * H + h], bias, prm.dt_softplus)
-                                 : 0.f;
-        const float av = d * a2;
-        if (k < q) {
-          float sum = av;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-          pre += sum;
-        }
-        if (k == q) {
-          own_dt = d;
-          own_a = av;
-        }
-      }
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float nb = __shfl_up_sync(0xffffffffu, own_a, off);
-        if (lane >= off) own_a += nb;
-      }
-      dt_s[b * QT + r] = own_dt;
-      cs_s[b * QT + r] = pre + own_a;
+    constexpr int CPH = PB / 16;           // 16-byte chunks of a row per warp half
+    for (int c = 0; c < nch; ++c) {
+      const int sx = c % NX, b = c % NB;
+      if (!wwait(&pro_full[b], (c / NB) & 1)) break;
+      if (!wwait(cb_full, c & 1)) break;
+      if (!wwait(&x_full[sx], (c / NX) & 1)) break;
+      tc_fence_after();
+      if (warp == 2) TRACE(c, 5);
+      const float* pb = pro + b * kProStride;
+      const float cs_i = pb[kProCs + r];
+      // both column blocks of this warp are read from TMEM before one wait
+      const int nblk = (hf <= q) + (hf + 2 <= q);
+      float v[2][32];
+      if (nblk == 2)
+        tmem_ld32x2(tmem + lrow + kColCB + hf * 32, tmem + lrow + kColCB + (hf + 2) * 32, v[0],
+                    v[1]);
+      else if (nblk == 1)
+        tmem_ld32(tmem + lrow + kColCB + hf * 32, v[0]);
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pro_full[b]);
-      return true;
-    };
-
-    // state rows n = r, channels p0 + hf*PH + k
-    float hreg[PH];
-    const bool has_init =
-        prm.init && (prm.has_init == nullptr || prm.has_init[s] != 0);
+      if (lane == 0) mbar_arrive(cb_empty);
+      uint32_t pk[2][16];
 #pragma unroll
-    for (int k = 0; k < PH; ++k)
-      hreg[k] = has_init ? prm.init[((size_t)s * H + h) * PN + (size_t)(p0 + hf * PH + k) * NSTATE + r]
-                         : 0.f;
-    auto write_hT = [&]() {
+      for (int jj = 0; jj < 2; ++jj) {
+        const int jb = hf + 2 * jj;  // 32-column block
+        if (jb > q) {
 #pragma unroll
-      for (int k8 = 0; k8 < PH / 8; ++k8) {
+          for (int e = 0; e < 16; ++e) pk[jj][e] = 0u;
+          continue;
+        }
+        float* m = v[jj];  // the mask is formed in place of C.B^T
+        if (pb[kProSafe + jb] != 0.f) {
+          const float rowf = ex2(cs_i - pb[kProCs + 32 * jb]);
+          const float4* cf = reinterpret_cast<const float4*>(pb + kProColf + 32 * jb);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 f = cf[e4];
+            m[4 * e4 + 0] *= rowf * f.x;
+            m[4 * e4 + 1] *= rowf * f.y;
+            m[4 * e4 + 2] *= rowf * f.z;
+            m[4 * e4 + 3] *= rowf * f.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = 32 * jb + e;
+            m[e] *= ex2(cs_i - pb[kProCs + j]) * pb[kProDt + j];
+          }
+        }
+        if (jb == q) {  // causal mask on the diagonal block
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e > lane) m[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[jj][e] = pack_bf16(m[2 * e], m[2 * e + 1]);
+      }
+      if (warp == 2) TRACE(c, 12);
+      // M and w o x of the previous chunk are free once its Y and S products are done
+      if (c >= 1 && !wwait(ys_full, (c - 1) & 1)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+        tmem_st16(tmem + lrow + kColM + (hf + 2 * jj) * 16, pk[jj]);
+      // w o x for token row j = r: logical 16-byte chunks of this half, at their
+      // swizzled positions (the same in x and in w o x)
+      {
+        const float w = pb[kProW + r];
+        const uint8_t* xt = sm + L::kX + sx * L::kXPad;
+#pragma unroll
+        for (int k = 0; k < CPH; ++k) {
+          const uint32_t off = swz((uint32_t)(r * L::kXRow + 16 * (hf * CPH + k)), L::kSwB);
+          uint4 xv = *reinterpret_cast<const uint4*>(xt + off);
+          __nv_bfloat162* e2 = reinterpret_cast<__nv_bfloat162*>(&xv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(e2[e]);
+            e2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+          }
+          *reinterpret_cast<uint4*>(sm + L::kXs + off) = xv;
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(m_ready);
+        mbar_arrive(&x_empty[sx]);
+        mbar_arrive(&pro_empty[b]);
+      }
+      if (warp == 2) TRACE(c, 6);
+    }
+  } else {
+    // ------------------------------------------------------------ output warps
+    const int q = warp & 3;
+    const int r = 32 * q + lane;           // token row i of y, state row n of h
+    const uint32_t lrow = (uint32_t)(32 * q) << 16;
+    float hreg[PB];                        // h[n = r][p0 + k]
+    const bool has_init = prm.init && (prm.has_init == nullptr || prm.has_init[s] != 0);
+#pragma unroll
+    for (int k = 0; k < PB; ++k)
+      hreg[k] = has_init ? prm.init[((size_t)s * H + h) * PN + (size_t)(p0 + k) * NSTATE + r] : 0.f;
+    // h_j goes to h^T buffer j & 1 (h_{-1}, the initial state, to buffer 1)
+    auto write_hT = [&](int buf) {
+      uint8_t* ht = sm + L::kHT + buf * L::kHTPad;
+#pragma unroll
+      for (int k8 = 0; k8 < PB / 8; ++k8) {
         uint4 v;
         v.x = pack_bf16(hreg[8 * k8 + 0], hreg[8 * k8 + 1]);
         v.y = pack_bf16(hreg[8 * k8 + 2], hreg[8 * k8 + 3]);
         v.z = pack_bf16(hreg[8 * k8 + 4], hreg[8 * k8 + 5]);
         v.w = pack_bf16(hreg[8 * k8 + 6], hreg[8 * k8 + 7]);
-        const uint32_t off = swz((uint32_t)(r * L::kXRow + 16 * (hf * PH / 8 + k8)), L::kSwB);
-        *reinterpret_cast<uint4*>(sm + L::kHT + off) = v;
+        *reinterpret_cast<uint4*>(ht + swz((uint32_t)(r * L::kXRow + 16 * k8), L::kSwB)) = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(h_ready);
+      if (lane == 0) mbar_arrive(&h_ready[buf]);
     };
-    write_hT();
-
-    bool ok = (nch == 0) || prologue(0);
-    for (int c = 0; ok && c < nch; ++c) {
-      const int st = c % NST, b = c & 1;
-      const uint8_t* xt = sm + st * L::kStage + L::kStageX;
-      if (!(ok = ewait(&full[st], (c / NST) & 1))) break;
-      if (!(ok = ewait(&pro_full[b], (c >> 1) & 1))) break;
-      if (!(ok = ewait(&cb_full[b], (c >> 1) & 1))) break;
+    write_hT(1);
+    const float Dh = prm.D ? prm.D[h] : 0.f;
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const int b = c % NB, sx = c % NX;
+      if (!(ok = wwait(&pro_full[b], (c / NB) & 1))) break;
+      if (!(ok = wwait(ys_full, c & 1))) break;
       tc_fence_after();
-      const float* dtb = dt_s + b * QT;
-      const float* csb = cs_s + b * QT;
-      const float cs_i = csb[r];
-      const float cs_last = csb[QT - 1];
-      const float dt_r = dtb[r];
-
-      // (b) decay mask: M[i, j] = CB[i, j] 2^(cs_i - cs_j) dt_j for j <= i, bf16 into TMEM
+      if (warp == 2 + kMaskWarps) TRACE(c, 7);
+      const float* pb = pro + b * kProStride;
+      // state first: h = 2^cs_last h + S, then h^T for the next chunk's Yoff
+      const float e_l = ex2(pb[kProCs + QT - 1]);
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int jb = hf + 2 * jj;  // 32-column block
-        uint32_t pk[16];
-        if (jb > q) {
+      for (int sl = 0; sl < PB / 16; ++sl) {
+        float sv[16];
+        tmem_ld16(tmem + lrow + L::kS + 16 * sl, sv);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = 0u;
-        } else {
-          float v[32];
-          tmem_ld32(tmem + lrow + kColCB + b * 128 + jb * 32, v);
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int j = jb * 32 + e;
-            float m0 = v[e] * ex2(cs_i - csb[j]) * dtb[j];
-            float m1 = v[e + 1] * ex2(cs_i - csb[j + 1]) * dtb[j + 1];
-            if (jb == q && e > lane) m0 = 0.f;
-            if (jb == q && e + 1 > lane) m1 = 0.f;
-            pk[e / 2] = pack_bf16(m0, m1);
-          }
-        }
-        tmem_st16(tmem + lrow + kColM + jb * 16, pk);
+        for (int e = 0; e < 16; ++e) hreg[16 * sl + e] = fmaf(e_l, hreg[16 * sl + e], sv[e]);
       }
-      tmem_st_wait();
-
-      // (c) w o x for token row j = r: 16-byte chunks, the swizzle only permutes chunks
-      //     within a row, so the row is scaled in place of its physical chunks
-      {
-        const float w = ex2(cs_last - cs_i) * dt_r;
-        const uint4* src = reinterpret_cast<const uint4*>(xt + r * L::kXRow);
-        uint4* dst = reinterpret_cast<uint4*>(sm + L::kXs + r * L::kXRow);
-        constexpr int CPH = PB / 16;  // chunks per half row
-#pragma unroll
-        for (int k = 0; k < CPH; ++k) {
-          uint4 v = src[hf * CPH + k];
-          __nv_bfloat162* e2 = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float2 f = __bfloat1622float2(e2[e]);
-            e2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
-          }
-          dst[hf * CPH + k] = v;
-        }
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&cb_empty[b]);
-        mbar_arrive(m_ready);
-      }
-
-      // next chunk's dt / cumsum while the tensor core runs
-      if (c + 1 < nch && !(ok = prologue(c + 1))) break;
-
-      // (d) y = Y + 2^cs_i Yoff + D x, rows i = r, channels of this half
-      if (!(ok = ewait(acc_full, c & 1))) break;
-      if (!(ok = ewait(yoff_full, c & 1))) break;
+      if (lane == 0) mbar_arrive(s_empty);
+      if (c + 1 < nch) write_hT(c & 1);
+      // then y = Y + 2^cs_i Yoff + D x
+      if (!(ok = wwait(&yoff_full[c & 1], (c >> 1) & 1))) break;
+      if (!(ok = wwait(&x_full[sx], (c / NX) & 1))) break;
       tc_fence_after();
-      {
-        float yv[PH], yo[PH];
-        tmem_ld<PH>(tmem + lrow + kColY + hf * PH, yv);
-        tmem_ld<PH>(tmem + lrow + kColY + PB + hf * PH, yo);
-        const float e_i = ex2(cs_i);
-        const int tok = t0 + c * QT + r;
+      const float e_i = ex2(pb[kProCs + r]);
+      const int tok = t0 + c * QT + r;
+      __nv_bfloat16* yrow = prm.y + ((size_t)tok * H + h) * P + p0;
+      const uint8_t* xt = sm + L::kX + sx * L::kXPad;
+      const uint32_t colY = tmem + lrow + L::kY0 + (c & 1) * PB;
+      const uint32_t colO = tmem + lrow + L::kO0 + (c & 1) * PB;
 #pragma unroll
-        for (int k8 = 0; k8 < PH / 8; ++k8) {
-          const uint32_t off = swz((uint32_t)(r * L::kXRow + 16 * (hf * PH / 8 + k8)), L::kSwB);
-          uint4 xv = *reinterpret_cast<const uint4*>(xt + off);
-          const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
-          uint4 o;
-          uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+      for (int sl = 0; sl < PB / 16; ++sl) {
+        float yv[16], yo[16];
+        tmem_ld16x2(colY + 16 * sl, colO + 16 * sl, yv, yo);
+        uint4 xr[2];
+        xr[0] = *reinterpret_cast<const uint4*>(xt + swz((uint32_t)(r * L::kXRow + 32 * sl), L::kSwB));
+        xr[1] = *reinterpret_cast<const uint4*>(xt + swz((uint32_t)(r * L::kXRow + 32 * sl + 16), L::kSwB));
+        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(xr);
+        uint4 o[2];
+        uint32_t* o32 = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 xf = __bfloat1622float2(x2[e]);
-            const int k = 8 * k8 + 2 * e;
-            const float y0 = fmaf(e_i, yo[k], yv[k]) + Dh * xf.x;
-            const float y1 = fmaf(e_i, yo[k + 1], yv[k + 1]) + Dh * xf.y;
-            o32[e] = pack_bf16(y0, y1);
-          }
-          if (tok < t1)
-            *reinterpret_cast<uint4*>(prm.y + ((size_t)tok * H + h) * P + p0 + hf * PH + 8 * k8) = o;
+        for (int e = 0; e < 8; ++e) {
+          const float2 xf = __bfloat1622float2(x2[e]);
+          o32[e] = pack_bf16(fmaf(e_i, yo[2 * e], yv[2 * e]) + Dh * xf.x,
+                             fmaf(e_i, yo[2 * e + 1], yv[2 * e + 1]) + Dh * xf.y);
         }
-      }
-      // (e) state pass: h = 2^cs_last h + S, rows n = r
-      {
-        float sv[PH];
-        tmem_ld<PH>(tmem + lrow + kColY + 2 * PB + hf * PH, sv);
-        const float e_l = ex2(cs_last);
-#pragma unroll
-        for (int k = 0; k < PH; ++k) hreg[k] = fmaf(e_l, hreg[k], sv[k]);
+        if (tok < t1) {
+          reinterpret_cast<uint4*>(yrow + 16 * sl)[0] = o[0];
+          reinterpret_cast<uint4*>(yrow + 16 * sl)[1] = o[1];
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(acc_empty);
+        mbar_arrive(&y_empty[c & 1]);
+        mbar_arrive(&x_empty[sx]);
         mbar_arrive(&pro_empty[b]);
-        mbar_arrive(&empty[st]);
       }
-      if (c + 1 < nch) write_hT();
+      if (warp == 2 + kMaskWarps) TRACE(c, 8);
     }
     if (ok && fin) {
 #pragma unroll
-      for (int k = 0; k < PH; ++k) fin[(size_t)(hf * PH + k) * NSTATE + r] = hreg[k];
+      for (int k = 0; k < PB; ++k) fin[(size_t)k * NSTATE + r] = hreg[k];
     }
   }
 
@@ -470,6 +637,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0 && *abort_flag) set_status(prm.status, SSD_DEV_TIMEOUT);
 }
+
+#ifdef SSD_TRACE
+}  // namespace
+extern "C" SSD_API int ssd_trace_read(long long* dst) {
+  return (int)cudaMemcpyFromSymbol(dst, g_trace, sizeof(g_trace));
+}
+namespace {
+#endif
 
 // ------------------------------------------------------------------ host side
 
