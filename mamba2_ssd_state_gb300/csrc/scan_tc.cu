@@ -19,13 +19,15 @@
 // workload has few (sequence, head) pairs.
 //
 // Warp roles (480 threads), pipelined across chunks:
-//   warp 0      TMA producer (one lane): C and B of a chunk (two 64-wide 128B-swizzled
-//               boxes each) into a 2-deep ring freed by the tensor core, x into a ring
-//               freed by the mask and output warps, plus L2 prefetches further ahead.
+//   warp 0      TMA producer (one lane): B and C of a chunk (two 64-wide 128B-swizzled
+//               boxes each) into their own rings, freed by the tensor core as soon as
+//               their last product is done, x into a ring freed by the mask and output
+//               warps, plus L2 prefetches further ahead.
 //   warp 1      TMEM owner (512 columns); one lane issues every MMA, in whatever order
 //               their inputs become ready.
-//   warps 2-9   mask warps (two per TMEM lane quadrant): C.B^T -> M (bf16, written
-//               back to TMEM as the A operand of Y = M x) and w o x into shared memory.
+//   warps 2-9   mask warps (two per TMEM lane quadrant): first w o x into shared memory
+//               (so the chunk state S, which needs no mask, starts early and frees B),
+//               then C.B^T -> M (bf16, written back to TMEM as the A operand of Y = M x).
 //   warps 10-13 output warps (one per quadrant): first the state, h = 2^cs_last h + S
 //               in fp32 registers and h^T (bf16) for the next chunk's Yoff, then
 //               y = Y + 2^cs_i Yoff + D x, then the final state.
@@ -59,7 +61,7 @@ using namespace tc;
 
 constexpr int QT = 128;          // chunk length = tcgen05 M
 constexpr int NSTATE = 128;      // state size N of this kernel
-constexpr int NBC = 2;           // TMA ring depth of B and C
+constexpr int NBB = 2;           // TMA ring depth of B
 constexpr int NB = 3;            // depth of the decay buffer ring
 constexpr int kMaskWarps = 8, kOutWarps = 4;
 constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
@@ -102,18 +104,19 @@ struct TcParams {
 template <int PB>
 struct Layout {
   static constexpr int NX = PB == 64 ? 2 : 3;          // TMA ring depth of x
+  static constexpr int NBC = PB == 64 ? 2 : 3;         // TMA ring depth of C
   static constexpr int kXRow = PB * 2;                 // bytes per token row of x / x' / h^T
   static constexpr int kXBytes = QT * kXRow;
   static constexpr int kXPad = (kXBytes + 1023) / 1024 * 1024;
-  static constexpr int kBC = 0;                        // NBC x (C: 32 KB, B: 32 KB)
-  static constexpr int kBCStage = 65536;
-  static constexpr int kX = NBC * kBCStage;            // NX x x tile
+  static constexpr int kB = 0;                         // NBB x B tile (two [128 x 64] boxes)
+  static constexpr int kC = NBB * 32768;               // NBC x C tile
+  static constexpr int kX = kC + NBC * 32768;          // NX x x tile
   static constexpr int kXs = kX + NX * kXPad;          // w o x
   static constexpr int kHT = kXs + kXPad;              // h^T x 2, [N rows][PB] bf16 each
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
   static constexpr int kPro = kHT + 2 * kHTPad;        // float [NB][kProStride]
   static constexpr int kBar = kPro + NB * kProStride * 4;
-  static constexpr int kNumBar = 2 * NBC + 2 * NX + 2 * NB + 12;
+  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 15;
   static constexpr int kFlags = kBar + kNumBar * 8;    // abort flag, TMEM base
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams prm) {
   using L = Layout<PB>;
-  constexpr int NX = L::NX;
+  constexpr int NX = L::NX, NBC = L::NBC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
@@ -172,9 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   float* pro = reinterpret_cast<float*>(sm + L::kPro);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
-  uint64_t* bc_full = bars;                 // [NBC] B, C landed
-  uint64_t* bc_empty = bc_full + NBC;       // [NBC] B, C free (MMA commit after Yoff)
-  uint64_t* x_full = bc_empty + NBC;        // [NX]  x landed
+  uint64_t* b_full = bars;                  // [NBB] B landed
+  uint64_t* b_empty = b_full + NBB;         // [NBB] B free (MMA commit after S)
+  uint64_t* c_full = b_empty + NBB;         // [NBC] C landed
+  uint64_t* c_empty = c_full + NBC;         // [NBC] C free (MMA commit after Yoff)
+  uint64_t* x_full = c_empty + NBC;         // [NX]  x landed
   uint64_t* x_empty = x_full + NX;          // [NX]  x free (8 mask + 4 output warps)
   uint64_t* pro_full = x_empty + NX;        // [NB]  decay of a chunk ready (decay warp)
   uint64_t* pro_empty = pro_full + NB;      // [NB]  consumed (8 mask + 4 output warps)
@@ -182,20 +187,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barrier per buffer, so no waiter can fall two phases behind its barrier.
   uint64_t* cb_full = pro_empty + NB;       //       C.B^T in TMEM
   uint64_t* cb_empty = cb_full + 1;         //       C.B^T read (8 mask warps)
-  uint64_t* m_ready = cb_full + 2;          //       M in TMEM, w o x in smem (8 mask warps)
-  uint64_t* ys_full = cb_full + 3;          //       Y and S done (frees M and w o x)
+  uint64_t* xs_ready = cb_full + 2;         //       w o x in smem (8 mask warps)
+  uint64_t* s_full = cb_full + 3;           //       S done (also frees w o x)
   uint64_t* s_empty = cb_full + 4;          //       S read (4 output warps)
-  uint64_t* h_ready = cb_full + 5;          // [2]   h^T buffer written (4 output warps)
-  uint64_t* yoff_full = cb_full + 7;        // [2]   Yoff buffer done
-  uint64_t* y_empty = cb_full + 9;          // [2]   Y and Yoff buffers read (4 output warps)
-  uint64_t* drain = cb_full + 11;           //       teardown: all MMAs retired
+  uint64_t* m_ready = cb_full + 5;          //       M in TMEM (8 mask warps)
+  uint64_t* y_full = cb_full + 6;           // [2]   Y buffer done (also frees M)
+  uint64_t* h_ready = cb_full + 8;          // [2]   h^T buffer written (4 output warps)
+  uint64_t* yoff_full = cb_full + 10;       // [2]   Yoff buffer done
+  uint64_t* y_empty = cb_full + 12;         // [2]   Y and Yoff buffers read (4 output warps)
+  uint64_t* drain = cb_full + 14;           //       teardown: all MMAs retired
+  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 15,
+                "barrier block size must match the barriers laid out here");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < NBB; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
     for (int i = 0; i < NBC; ++i) {
-      mbar_init(&bc_full[i], 1);
-      mbar_init(&bc_empty[i], 1);
+      mbar_init(&c_full[i], 1);
+      mbar_init(&c_empty[i], 1);
     }
     for (int i = 0; i < NX; ++i) {
       mbar_init(&x_full[i], 1);
@@ -207,10 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(cb_full, 1);
     mbar_init(cb_empty, kMaskWarps);
-    mbar_init(m_ready, kMaskWarps);
-    mbar_init(ys_full, 1);
+    mbar_init(xs_ready, kMaskWarps);
+    mbar_init(s_full, 1);
     mbar_init(s_empty, kOutWarps);
+    mbar_init(m_ready, kMaskWarps);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&y_full[i], 1);
       mbar_init(&h_ready[i], kOutWarps);
       mbar_init(&yoff_full[i], 1);
       mbar_init(&y_empty[i], kOutWarps);
@@ -239,47 +254,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (lane 0)
     if (lane == 0) {
-      constexpr int kAhead = 2;  // L2 prefetch distance beyond the rings, in chunks
-      for (int c = 0; c < NBC + kAhead && c < nch; ++c) {
+      constexpr int kAhead = 4;  // L2 prefetch distance, in chunks
+      auto prefetch = [&](int c) {
         const int tok = t0 + c * QT;
-        tma_prefetch_3d(&tmC, 0, g, tok);
-        tma_prefetch_3d(&tmC, 64, g, tok);
         tma_prefetch_3d(&tmB, 0, g, tok);
         tma_prefetch_3d(&tmB, 64, g, tok);
+        tma_prefetch_3d(&tmC, 0, g, tok);
+        tma_prefetch_3d(&tmC, 64, g, tok);
         tma_prefetch_3d(&tmX, p0, h, tok);
-      }
-      int bc_issued = 0, x_issued = 0;
+      };
+      for (int c = 0; c < kAhead && c < nch; ++c) prefetch(c);
+      int nb_iss = 0, nc_iss = 0, nx_iss = 0;
       for (int c = 0; c < nch; ++c) {
         const int tok = t0 + c * QT;
-        const int sb = c % NBC, sx = c % NX;
-        if (c >= NBC && !mbar_wait(&bc_empty[sb], ((c / NBC) - 1) & 1, abort_flag, kWaitLimit))
+        if (c + kAhead < nch) prefetch(c + kAhead);
+        const int sb = c % NBB, sc = c % NBC, sx = c % NX;
+        if (c >= NBB && !mbar_wait(&b_empty[sb], ((c / NBB) - 1) & 1, abort_flag, kWaitLimit))
           break;
-        uint8_t* bc = sm + L::kBC + sb * L::kBCStage;
-        mbar_arrive_expect_tx(&bc_full[sb], 65536);
-        tma_load_3d(bc, &tmC, &bc_full[sb], 0, g, tok);
-        tma_load_3d(bc + 16384, &tmC, &bc_full[sb], 64, g, tok);
-        tma_load_3d(bc + 32768, &tmB, &bc_full[sb], 0, g, tok);
-        tma_load_3d(bc + 49152, &tmB, &bc_full[sb], 64, g, tok);
-        bc_issued = c + 1;
-        if (c + NBC + kAhead < nch) {
-          const int tp = tok + (NBC + kAhead) * QT;
-          tma_prefetch_3d(&tmC, 0, g, tp);
-          tma_prefetch_3d(&tmC, 64, g, tp);
-          tma_prefetch_3d(&tmB, 0, g, tp);
-          tma_prefetch_3d(&tmB, 64, g, tp);
-          tma_prefetch_3d(&tmX, p0, h, tp);
-        }
+        uint8_t* bt = sm + L::kB + sb * 32768;
+        mbar_arrive_expect_tx(&b_full[sb], 32768);
+        tma_load_3d(bt, &tmB, &b_full[sb], 0, g, tok);
+        tma_load_3d(bt + 16384, &tmB, &b_full[sb], 64, g, tok);
+        nb_iss = c + 1;
+        if (c >= NBC && !mbar_wait(&c_empty[sc], ((c / NBC) - 1) & 1, abort_flag, kWaitLimit))
+          break;
+        uint8_t* ct = sm + L::kC + sc * 32768;
+        mbar_arrive_expect_tx(&c_full[sc], 32768);
+        tma_load_3d(ct, &tmC, &c_full[sc], 0, g, tok);
+        tma_load_3d(ct + 16384, &tmC, &c_full[sc], 64, g, tok);
+        nc_iss = c + 1;
         if (c >= NX && !mbar_wait(&x_empty[sx], ((c / NX) - 1) & 1, abort_flag, kWaitLimit))
           break;
         mbar_arrive_expect_tx(&x_full[sx], L::kXBytes);
         tma_load_3d(sm + L::kX + sx * L::kXPad, &tmX, &x_full[sx], p0, h, tok);
-        x_issued = c + 1;
+        nx_iss = c + 1;
         TRACE(c, 0);
       }
       // every copy issued must have landed before the CTA's shared memory is released
-      for (int c = bc_issued > NBC ? bc_issued - NBC : 0; c < bc_issued; ++c)
-        mbar_wait_drain(&bc_full[c % NBC], (c / NBC) & 1, kWaitLimit);
-      for (int c = x_issued > NX ? x_issued - NX : 0; c < x_issued; ++c)
+      for (int c = nb_iss > NBB ? nb_iss - NBB : 0; c < nb_iss; ++c)
+        mbar_wait_drain(&b_full[c % NBB], (c / NBB) & 1, kWaitLimit);
+      for (int c = nc_iss > NBC ? nc_iss - NBC : 0; c < nc_iss; ++c)
+        mbar_wait_drain(&c_full[c % NBC], (c / NBC) & 1, kWaitLimit);
+      for (int c = nx_iss > NX ? nx_iss - NX : 0; c < nx_iss; ++c)
         mbar_wait_drain(&x_full[c % NX], (c / NX) & 1, kWaitLimit);
     }
   } else if (warp == kDecayWarp) {
@@ -354,70 +370,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idY = make_idesc_bf16(128, PB, false, true);
       constexpr uint32_t idS = make_idesc_bf16(128, PB, true, true);
       constexpr uint32_t idO = make_idesc_bf16(128, PB, false, true);
-      const uint32_t sXs = smem_u32(sm + L::kXs);
+      // Descriptors are built once; a K step only advances the start-address field
+      // (bits 0-13, in 16-byte units), which stays inside the field for every tile here.
+      auto kstep_k = [](int kk) -> uint64_t {  // K-major, 128B swizzle: 64-wide K blocks
+        return (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4));
+      };
+      // per-buffer descriptors: the buffers of a ring are evenly spaced, so buffer i's
+      // descriptor is buffer 0's plus i times the spacing (in 16-byte units)
+      const uint64_t dB_k0 = make_sdesc(smem_u32(sm + L::kB), 16, 1024, kSw128);
+      const uint64_t dB_mn0 = make_sdesc(smem_u32(sm + L::kB), 16384, 1024, kSw128);
+      const uint64_t dC_k0 = make_sdesc(smem_u32(sm + L::kC), 16, 1024, kSw128);
+      const uint64_t dX0 = make_sdesc(smem_u32(sm + L::kX), L::kXBytes, 8 * L::kXRow, L::kSwCode);
+      const uint64_t dHT0 = make_sdesc(smem_u32(sm + L::kHT), L::kHTPad, 8 * L::kXRow, L::kSwCode);
+      const uint64_t dXs = make_sdesc(smem_u32(sm + L::kXs), L::kXBytes, 8 * L::kXRow, L::kSwCode);
       // Issue whichever product is ready, each kind in chunk order:
       //   CB(k)    B, C of k landed; C.B^T of k-1 read by the mask warps
-      //   Y,S(k)   M and w o x of k; Y buffer of k-2 and S of k-1 read
-      //   Yoff(k)  Y,S(k) issued; h^T = h_{k-1}; Yoff buffer of k-2 read
-      int ncb = 0, nys = 0, nyo = 0;
+      //   S(k)     CB(k) issued; w o x of k; S of k-1 read          -> frees B of k
+      //   Yoff(k)  CB(k) issued; h^T = h_{k-1}; Yoff buffer of k-2 read -> frees C of k
+      //   Y(k)     M of k; Y buffer of k-2 read
+      int ncb = 0, ns = 0, nyo = 0, ny = 0;
       long long t_idle = 0;
-      while (nyo < nch) {
+      while (ns < nch || ny < nch || nyo < nch) {
         bool progress = false;
-        if (ncb < nch && mbar_test_wait(&bc_full[ncb % NBC], (ncb / NBC) & 1) &&
-            (ncb == 0 || mbar_test_wait(cb_empty, (ncb - 1) & 1))) {
+        if (ns < ncb && mbar_test_wait(xs_ready, ns & 1) &&
+            (ns == 0 || mbar_test_wait(s_empty, (ns - 1) & 1))) {
           tc_fence_after();
-          const uint32_t sC = smem_u32(sm + L::kBC + (ncb % NBC) * L::kBCStage);
-          const uint32_t sB = sC + 32768;
+          // S^T = B^T (w o x): A = B read MN-major, 16 token rows (2 KB) per K step
+          const uint64_t da = dB_mn0 + (uint64_t)((ns % NBB) * (32768 >> 4));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // K = N = 128 in steps of 16 (32 bytes)
-            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + kColCB, make_sdesc(sC + ko, 16, 1024, kSw128),
-                   make_sdesc(sB + ko, 16, 1024, kSw128), idCB, kk > 0);
-          }
-          mma_commit(cb_full);
-          ++ncb;
-          progress = true;
-        }
-        if (nys < ncb && mbar_test_wait(m_ready, nys & 1) &&
-            mbar_test_wait(&x_full[nys % NX], (nys / NX) & 1) &&
-            (nys < 1 || mbar_test_wait(s_empty, (nys - 1) & 1)) &&
-            (nys < 2 || mbar_test_wait(&y_empty[nys & 1], ((nys >> 1) - 1) & 1))) {
-          tc_fence_after();
-          TRACE(nys, 3);
-          const uint32_t sX = smem_u32(sm + L::kX + (nys % NX) * L::kXPad);
-          const uint32_t sB = smem_u32(sm + L::kBC + (nys % NBC) * L::kBCStage) + 32768;
-          const uint32_t colY = tmem + L::kY0 + (nys & 1) * PB;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // Y = M x : K = 128 tokens, M from TMEM (8 cols/step)
-            mma_ts(colY, tmem + kColM + kk * 8,
-                   make_sdesc(sX + kk * 16 * L::kXRow, L::kXBytes, 8 * L::kXRow, L::kSwCode), idY,
-                   kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // S^T = B^T (w o x): A = B read MN-major
-            mma_ss(tmem + L::kS, make_sdesc(sB + kk * 2048, 16384, 1024, kSw128),
-                   make_sdesc(sXs + kk * 16 * L::kXRow, L::kXBytes, 8 * L::kXRow, L::kSwCode),
-                   idS, kk > 0);
-          mma_commit(ys_full);
-          ++nys;
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + L::kS, da + kk * 128, dXs + kk * L::kXRow, idS, kk > 0);
+          mma_commit(s_full);
+          mma_commit(&b_empty[ns % NBB]);
+          TRACE(ns, 9);
+          ++ns;
           progress = true;
         }
         // h_j sits in h^T buffer j & 1 as that buffer's ((j + 1) >> 1)-th value
-        if (nyo < nys && mbar_test_wait(&h_ready[(nyo + 1) & 1], (nyo >> 1) & 1) &&
+        if (nyo < ncb && mbar_test_wait(&h_ready[(nyo + 1) & 1], (nyo >> 1) & 1) &&
             (nyo < 2 || mbar_test_wait(&y_empty[nyo & 1], ((nyo >> 1) - 1) & 1))) {
           tc_fence_after();
           TRACE(nyo, 4);
-          const uint32_t sC = smem_u32(sm + L::kBC + (nyo % NBC) * L::kBCStage);
-          const uint32_t sHT = smem_u32(sm + L::kHT + ((nyo + 1) & 1) * L::kHTPad);  // h_{k-1}
+          const uint64_t da = dC_k0 + (uint64_t)((nyo % NBC) * (32768 >> 4));
+          const uint64_t db = dHT0 + (uint64_t)(((nyo + 1) & 1) * (L::kHTPad >> 4));  // h_{k-1}
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // Yoff = C h^T : K = N = 128
-            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + L::kO0 + (nyo & 1) * PB, make_sdesc(sC + ko, 16, 1024, kSw128),
-                   make_sdesc(sHT + kk * 16 * L::kXRow, L::kHTPad, 8 * L::kXRow, L::kSwCode), idO,
+          for (int kk = 0; kk < 8; ++kk)  // Yoff = C h^T : K = N = 128
+            mma_ss(tmem + L::kO0 + (nyo & 1) * PB, da + kstep_k(kk), db + kk * L::kXRow, idO,
                    kk > 0);
-          }
           mma_commit(&yoff_full[nyo & 1]);
-          mma_commit(&bc_empty[nyo % NBC]);
+          mma_commit(&c_empty[nyo % NBC]);
           ++nyo;
+          progress = true;
+        }
+        if (ncb < nch && mbar_test_wait(&b_full[ncb % NBB], (ncb / NBB) & 1) &&
+            mbar_test_wait(&c_full[ncb % NBC], (ncb / NBC) & 1) &&
+            (ncb == 0 || mbar_test_wait(cb_empty, (ncb - 1) & 1))) {
+          tc_fence_after();
+          const uint64_t da = dC_k0 + (uint64_t)((ncb % NBC) * (32768 >> 4));
+          const uint64_t db = dB_k0 + (uint64_t)((ncb % NBB) * (32768 >> 4));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // K = N = 128 in steps of 16 (32 bytes)
+            mma_ss(tmem + kColCB, da + kstep_k(kk), db + kstep_k(kk), idCB, kk > 0);
+          mma_commit(cb_full);
+          TRACE(ncb, 10);
+          ++ncb;
+          progress = true;
+        }
+        if (ny < ncb && mbar_test_wait(m_ready, ny & 1) &&
+            (ny < 2 || mbar_test_wait(&y_empty[ny & 1], ((ny >> 1) - 1) & 1))) {
+          tc_fence_after();
+          TRACE(ny, 3);
+          const uint64_t db = dX0 + (uint64_t)((ny % NX) * (L::kXPad >> 4));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // Y = M x : K = 128 tokens, M from TMEM (8 cols/step)
+            mma_ts(tmem + L::kY0 + (ny & 1) * PB, tmem + kColM + kk * 8, db + kk * L::kXRow, idY,
+                   kk > 0);
+          mma_commit(&y_full[ny & 1]);
+          ++ny;
           progress = true;
         }
         if (progress) {
@@ -430,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
             break;
           }
-          __nanosleep(20);
+          __nanosleep(32);
         }
       }
       mma_commit(drain);
@@ -446,14 +475,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nch; ++c) {
       const int sx = c % NX, b = c % NB;
       if (!wwait(&pro_full[b], (c / NB) & 1)) break;
-      if (!wwait(cb_full, c & 1)) break;
       if (!wwait(&x_full[sx], (c / NX) & 1)) break;
-      tc_fence_after();
-      if (warp == 2) TRACE(c, 5);
       const float* pb = pro + b * kProStride;
+      // (1) w o x for token row j = r: logical 16-byte chunks of this half at their
+      //     swizzled positions (the same in x and in w o x); the buffer is free once the
+      //     previous chunk's S product is done
+      if (c >= 1 && !wwait(s_full, (c - 1) & 1)) break;
+      if (warp == 2) TRACE(c, 5);
+      {
+        const float w = pb[kProW + r];
+        const uint8_t* xt = sm + L::kX + sx * L::kXPad;
+#pragma unroll
+        for (int k = 0; k < CPH; ++k) {
+          const uint32_t off = swz((uint32_t)(r * L::kXRow + 16 * (hf * CPH + k)), L::kSwB);
+          uint4 xv = *reinterpret_cast<const uint4*>(xt + off);
+          __nv_bfloat162* e2 = reinterpret_cast<__nv_bfloat162*>(&xv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(e2[e]);
+            e2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+          }
+          *reinterpret_cast<uint4*>(sm + L::kXs + off) = xv;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xs_ready);
+      if (warp == 2) TRACE(c, 14);
+      // (2) the decay mask from C.B^T
+      if (!wwait(cb_full, c & 1)) break;
+      tc_fence_after();
       const float cs_i = pb[kProCs + r];
-      // both column blocks of this warp are read from TMEM before one wait
-      const int nblk = (hf <= q) + (hf + 2 <= q);
+      const int nblk = (hf <= q) + (hf + 2 <= q);  // column blocks at or below the diagonal
       float v[2][32];
       if (nblk == 2)
         tmem_ld32x2(tmem + lrow + kColCB + hf * 32, tmem + lrow + kColCB + (hf + 2) * 32, v[0],
@@ -500,32 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) pk[jj][e] = pack_bf16(m[2 * e], m[2 * e + 1]);
       }
       if (warp == 2) TRACE(c, 12);
-      // M and w o x of the previous chunk are free once its Y and S products are done
-      if (c >= 1 && !wwait(ys_full, (c - 1) & 1)) break;
+      // M of the previous chunk is free once its Y product is done
+      if (c >= 1 && !wwait(&y_full[(c - 1) & 1], ((c - 1) >> 1) & 1)) break;
       tc_fence_after();
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj)
         tmem_st16(tmem + lrow + kColM + (hf + 2 * jj) * 16, pk[jj]);
-      // w o x for token row j = r: logical 16-byte chunks of this half, at their
-      // swizzled positions (the same in x and in w o x)
-      {
-        const float w = pb[kProW + r];
-        const uint8_t* xt = sm + L::kX + sx * L::kXPad;
-#pragma unroll
-        for (int k = 0; k < CPH; ++k) {
-          const uint32_t off = swz((uint32_t)(r * L::kXRow + 16 * (hf * CPH + k)), L::kSwB);
-          uint4 xv = *reinterpret_cast<const uint4*>(xt + off);
-          __nv_bfloat162* e2 = reinterpret_cast<__nv_bfloat162*>(&xv);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(e2[e]);
-            e2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
-          }
-          *reinterpret_cast<uint4*>(sm + L::kXs + off) = xv;
-        }
-      }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -567,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB, sx = c % NX;
       if (!(ok = wwait(&pro_full[b], (c / NB) & 1))) break;
-      if (!(ok = wwait(ys_full, c & 1))) break;
+      if (!(ok = wwait(s_full, c & 1))) break;
       tc_fence_after();
       if (warp == 2 + kMaskWarps) TRACE(c, 7);
       const float* pb = pro + b * kProStride;
@@ -584,10 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty);
       if (c + 1 < nch) write_hT(c & 1);
+      if (warp == 2 + kMaskWarps) TRACE(c, 11);
       // then y = Y + 2^cs_i Yoff + D x
+      if (!(ok = wwait(&y_full[c & 1], (c >> 1) & 1))) break;
       if (!(ok = wwait(&yoff_full[c & 1], (c >> 1) & 1))) break;
       if (!(ok = wwait(&x_full[sx], (c / NX) & 1))) break;
       tc_fence_after();
+      if (warp == 2 + kMaskWarps) TRACE(c, 13);
       const float e_i = ex2(pb[kProCs + r]);
       const int tok = t0 + c * QT + r;
       __nv_bfloat16* yrow = prm.y + ((size_t)tok * H + h) * P + p0;

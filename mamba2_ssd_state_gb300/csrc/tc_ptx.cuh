@@ -62,6 +62,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // that a broken pipeline ends the kernel instead of hanging the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           long long limit) {
+  if (mbar_test_wait(bar, parity)) return true;  // completed phases cost one test
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
