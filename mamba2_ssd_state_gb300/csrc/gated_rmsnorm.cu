@@ -61,44 +61,62 @@ template <> struct Vec8<float> {
   }
 };
 
-// group_size == VPT * 256: lane l holds elements [8 (l + 32 i), +8) for i < VPT, so each
-// load instruction of a warp covers 32 consecutive 8-element vectors (coalesced).
-template <typename TA, typename TW, int VPT>
+// group_size == TPG * 8 * VPT: the TPG threads of a group (one to eight warps) each hold
+// VPT 8-element vectors, thread t vectors t + TPG i, so every load instruction of a warp
+// covers 32 consecutive vectors (coalesced), and at most 4 vectors per thread keep the
+// register count low enough for several blocks per SM.  Warp partial sums meet in
+// shared memory when a group spans several warps.
+template <typename TA, typename TW, int VPT, int TPG>
 __global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
                                                        const TA* __restrict__ z,
                                                        const TW* __restrict__ w, TA* out,
                                                        int64_t units, int d, int gs, float eps) {
-  const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (unit >= units) return;
-  const int lane = threadIdx.x & 31;
+  constexpr int GPB = 256 / TPG;  // groups per block
+  __shared__ float part[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tig = threadIdx.x % TPG;
+  const int64_t unit = (int64_t)blockIdx.x * GPB + threadIdx.x / TPG;
+  const bool valid = unit < units;
   const int ngroups = d / gs;
-  const int64_t row = unit / ngroups;
-  const int col0 = (int)(unit % ngroups) * gs;
+  const int64_t row = valid ? unit / ngroups : 0;
+  const int col0 = valid ? (int)(unit % ngroups) * gs : 0;
   const size_t base = (size_t)row * d + col0;
   float g[VPT][8];
   float ss = 0.f;
+  if (valid) {
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int off = 8 * (lane + 32 * i);
-    float xv[8];
-    Vec8<TA>::load(x + base + off, xv);
-    if (z) {
-      float zv[8];
-      Vec8<TA>::load(z + base + off, zv);
+    for (int i = 0; i < VPT; ++i) {
+      const int off = 8 * (tig + TPG * i);
+      float xv[8];
+      Vec8<TA>::load(x + base + off, xv);
+      if (z) {
+        float zv[8];
+        Vec8<TA>::load(z + base + off, zv);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) g[i][e] = xv[e] * gate<TA>(zv[e]);
-    } else {
+        for (int e = 0; e < 8; ++e) g[i][e] = xv[e] * gate<TA>(zv[e]);
+      } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) g[i][e] = xv[e];
+        for (int e = 0; e < 8; ++e) g[i][e] = xv[e];
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(g[i][e], g[i][e], ss);
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(g[i][e], g[i][e], ss);
   }
   ss = warp_sum(ss);
+  if constexpr (TPG > 32) {
+    if (lane == 0) part[warp] = ss;
+    __syncthreads();
+    constexpr int WPG = TPG / 32;  // warps per group
+    const int w0 = (warp / WPG) * WPG;
+    ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < WPG; ++k) ss += part[w0 + k];
+  }
+  if (!valid) return;
   const float r = rsqrtf(ss / (float)gs + eps);
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int off = 8 * (lane + 32 * i);
+    const int off = 8 * (tig + TPG * i);
     float wv[8], o[8];
     Vec8<TW>::load(w + col0 + off, wv);
 #pragma unroll
@@ -149,25 +167,31 @@ cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out,
   const bool aligned = ((uintptr_t)x % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
                        (z == nullptr || (uintptr_t)z % 16 == 0) && ((uintptr_t)w % 16 == 0) &&
                        ((size_t)d * sizeof(TA)) % 16 == 0;
-  const int vpt = (aligned && gs % 256 == 0) ? gs / 256 : 0;
-#define SSD_NORM_CASE(V)                                                                   \
-  case V:                                                                                  \
-    norm_vec_kernel<TA, TW, V><<<(unsigned)blocks, 256, 0, st>>>(xp, zp, wp, op, units, d, \
-                                                                 gs, eps);                 \
-    break;
-  switch (vpt) {
-    SSD_NORM_CASE(1)
-    SSD_NORM_CASE(2)
-    SSD_NORM_CASE(3)
-    SSD_NORM_CASE(4)
-    SSD_NORM_CASE(5)
-    SSD_NORM_CASE(6)
-    SSD_NORM_CASE(8)
-    default:
-      norm_generic_kernel<TA, TW><<<(unsigned)blocks, 256, 0, st>>>(xp, zp, wp, op, units, d,
-                                                                    gs, eps);
+  // vector path: the smallest group of threads (32..256) with at most 4 vectors each
+  int tpg = 0, vpt = 0;
+  if (aligned && gs % 8 == 0) {
+    for (int t = 32; t <= 256; t *= 2) {
+      const int nvec = gs / 8;
+      if (nvec % t == 0 && nvec / t <= 4) {
+        tpg = t;
+        vpt = nvec / t;
+        break;
+      }
+    }
   }
+  const int gpb = tpg ? 256 / tpg : 8;
+  const int64_t vblocks = (units + gpb - 1) / gpb;
+#define SSD_NORM_CASE(V, T)                                                               \
+  if (vpt == V && tpg == T) {                                                              \
+    norm_vec_kernel<TA, TW, V, T><<<(unsigned)vblocks, 256, 0, st>>>(xp, zp, wp, op, units, \
+                                                                     d, gs, eps);           \
+    return cudaGetLastError();                                                             \
+  }
+  SSD_NORM_CASE(1, 32) SSD_NORM_CASE(2, 32) SSD_NORM_CASE(3, 32) SSD_NORM_CASE(4, 32)
+  SSD_NORM_CASE(3, 64) SSD_NORM_CASE(4, 64) SSD_NORM_CASE(3, 128) SSD_NORM_CASE(4, 128)
+  SSD_NORM_CASE(3, 256) SSD_NORM_CASE(4, 256)
 #undef SSD_NORM_CASE
+  norm_generic_kernel<TA, TW><<<(unsigned)blocks, 256, 0, st>>>(xp, zp, wp, op, units, d, gs, eps);
   return cudaGetLastError();
 }
 

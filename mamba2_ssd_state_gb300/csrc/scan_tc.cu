@@ -776,15 +776,24 @@ bool scan_tc_supported(const ssd_scan_args& a, int* pb_out) {
   if (pb) {
     if (a.P % pb) return false;
   } else {
-    // Fewest waves of CTAs over 148+ SMs, with a per-chunk cost model in which a CTA's
-    // time grows slowly with its channel block (the C.B^T product and the decay mask do
-    // not depend on it): cost(PB) ~ 1 + PB/64.
+    // One CTA per SM: fewest waves of CTAs over the SMs wins; a CTA's time per chunk
+    // grows only slowly with its channel block (the mask and C.B^T do not depend on it),
+    // measured roughly as 1 + PB/256.
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0, n = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+        sms = n;
+      else
+        sms = 148;
+    }
     double best = 1e30;
     for (int cand : {64, 32, 16}) {
       if (a.P % cand) continue;
       const long long ctas = (long long)a.nseq * a.H * (a.P / cand);
-      const long long waves = (ctas + 147) / 148;
-      const double cost = (double)waves * (1.0 + cand / 64.0);
+      const long long waves = (ctas + sms - 1) / sms;
+      const double cost = (double)waves * (1.0 + cand / 256.0);
       if (cost < best - 1e-9) {
         best = cost;
         pb = cand;
