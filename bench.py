@@ -137,6 +137,7 @@ def run_ours(args, rank, world, local_rank):
 
     from mamba2_ssd_state_gb300 import build as lib_build
     from mamba2_ssd_state_gb300 import inputs as I
+    from mamba2_ssd_state_gb300 import shard
     from mamba2_ssd_state_gb300 import ssd
 
     lib_build.build()
@@ -149,7 +150,9 @@ def run_ours(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
 
     w = I.WORKLOADS[WORKLOAD]
-    s = I.scan_workload(WORKLOAD)
+    # data parallel: rank r processes its own batch of the workload (sequences r*2, r*2+1
+    # of the global batch), drawn with its own seed; no collective on the data path
+    s = I.scan_workload(WORKLOAD, seed=w["seed"] + 17 * rank)
     H, P, G, N, T, nseq = s.H, s.P, s.G, s.N, s.T, s.nseq
     d = H * P
     x, dt, A, B, C, Dp, bias = (T_(s.x), T_(s.dt), T_(s.A), T_(s.B), T_(s.C), T_(s.D),
@@ -225,11 +228,7 @@ def run_ours(args, rank, world, local_rank):
     scan_ms = [e[0].elapsed_time(e[1]) for e in evs]
     norm_ms = [e[1].elapsed_time(e[2]) for e in evs]
     upd_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = shard.max_over_ranks(sum(step_ms), dev)
     tokens_per_step = T + nseq
     value = tokens_per_step * world * args.steps / (total_ms / 1e3)
 
@@ -276,11 +275,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = shard.max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = tokens_per_step * world * args.steps / (e2e_ms / 1e3)
 
     rc, bits = ssd.read_status(status)
