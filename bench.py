@@ -459,8 +459,8 @@ def profile_only(args):
         dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
         return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
 
-    if args.profile in ("scan", "scan_large", "norm"):
-        name = WORKLOAD if args.profile != "scan_large" else "nemotron_h_varlen"
+    if args.profile in ("scan", "scan_large", "norm", "norm_large"):
+        name = WORKLOAD if args.profile in ("scan", "norm") else "nemotron_h_varlen"
         s = I.scan_workload(name)
         x, dt, A, B, C, Dp, bias, init = (T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D,
                                                             s.dt_bias, s.initial_states))
@@ -468,8 +468,8 @@ def profile_only(args):
         cu = torch.from_numpy(s.cu_seqlens).to(dev)
         y = torch.empty_like(x)
         fs = torch.empty((s.nseq, s.H, s.P, s.N), dtype=torch.float32, device=dev)
-        if args.profile == "norm":
-            w = I.WORKLOADS[WORKLOAD]
+        if args.profile in ("norm", "norm_large"):
+            w = I.WORKLOADS[name]
             nrm = I.make_norm_inputs(s.T, s.H * s.P, w["norm_group"], act="bf16", seed=w["seed"] + 50)
             z, wt = T_(nrm.z), T_(nrm.weight)
             out = torch.empty((s.T, s.H * s.P), dtype=torch.bfloat16, device=dev)
@@ -480,7 +480,8 @@ def profile_only(args):
                                          D=Dp, dt_bias=bias, initial_states=init,
                                          has_initial_state=hi, y=y, final_states=fs)
     else:
-        H, P, G, N, S, batch = 128, 64, 8, 128, 512, 256
+        # a 96-slot pool (384 MiB, larger than L2) keeps a multi-pass capture small
+        H, P, G, N, S, batch = 128, 64, 8, 128, 96, 96
         idx = I.padded_permutation(S, batch, seed=3000 + batch)
         u = I.make_update_inputs(1, idx, H, P, G, N, act="bf16", seed=3100 + batch,
                                  pool_values=np.zeros((1, H, P, N), np.float32))
@@ -501,7 +502,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / large-scan legs")
-    ap.add_argument("--profile", choices=["scan", "scan_large", "norm", "update"],
+    ap.add_argument("--profile", choices=["scan", "scan_large", "norm", "norm_large", "update"],
                     help="only launch this op's benchmark workload steps times (for ncu)")
     args = ap.parse_args()
     if args.profile:

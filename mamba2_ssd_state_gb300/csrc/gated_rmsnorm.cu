@@ -14,9 +14,18 @@ namespace ssd {
 namespace {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
-// bf16 outputs carry 2^-9 relative rounding, far above the fast exponential's and
-// reciprocal's few-ulp error, so the bf16 path uses them; fp32 keeps expf and division.
-__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.f + __expf(-z)); }
+// bf16 outputs carry 2^-9 relative rounding, so the bf16 path evaluates the sigmoid as
+// 0.5 + 0.5 tanh(z/2) with the hardware tanh approximation (relative error about 2^-11,
+// one special-function op instead of an exponential and a reciprocal); fp32 keeps expf
+// and an IEEE division.
+__device__ __forceinline__ float tanh_approx(float v) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float silu_fast(float z) {
+  return z * fmaf(0.5f, tanh_approx(0.5f * z), 0.5f);
+}
 template <typename TA> __device__ __forceinline__ float gate(float z) {
   if constexpr (sizeof(TA) == 2) return silu_fast(z);
   else return silu(z);
