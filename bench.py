@@ -212,7 +212,11 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[3].record(stream)
 
-    launches_per_step = 3
+    # the scan is one launch, or three when the library splits the two sequences into
+    # segments (scan, combine, fix-up)
+    scan_split = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu,
+                                               chunk_size=s.chunk_size) > 0
+    launches_per_step = (3 if scan_split else 1) + 2
     for i in range(max(args.warmup, 3)):
         l2.flush()
         step()
@@ -256,7 +260,9 @@ def run_ours(args, rank, world, local_rank):
 
     sbytes = scan_bytes(T, H, P, G, N, nseq)
     scan_avg = sum(scan_ms) / len(scan_ms)
-    roof = {"bound": "hbm", "kernel": "scan_tc_kernel", "achieved": sbytes / (scan_avg / 1e3) / 1e9,
+    scan_kernels = ("scan_tc_kernel + scan_combine_kernel + scan_fixup_kernel" if scan_split
+                    else "scan_tc_kernel")
+    roof = {"bound": "hbm", "kernel": scan_kernels, "achieved": sbytes / (scan_avg / 1e3) / 1e9,
             "peak": hbm_peak, "unit": "GB/s", "peak_kind": f"{peak_kind} hbm copy",
             "algorithmic_bytes_per_launch": sbytes, "avg_launch_us": scan_avg * 1e3,
             "traffic": scan_traffic_from_profile(),
@@ -336,7 +342,8 @@ def run_ours(args, rank, world, local_rank):
 
 
 def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
-    """Decode at batch 256 on the 512-slot pool, and the large varlen prefill scan."""
+    """Decode at batch 256 on the 512-slot pool, the large varlen prefill scan and one long
+    sequence (split into segments by the library's planner)."""
     res = {}
     stream = torch.cuda.current_stream()
     H, P, G, N, S, batch = 128, 64, 8, 128, 512, 256
@@ -353,14 +360,14 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
     kw = dict(D=T_(u.D), dt_bias=T_(u.dt_bias))
     for _ in range(3):
         ssd.state_update(*args, **kw)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    e0.record(stream)
+    ev0.record(stream)
     for _ in range(iters):
         ssd.state_update(*args, **kw)
-    e1.record(stream)
+    ev1.record(stream)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / iters
+    us = ev0.elapsed_time(ev1) * 1e3 / iters
     active = int((idx >= 0).sum())
     ub = update_bytes(active, batch, H, P, G, N)
     res["decode_state_update"] = {
@@ -370,34 +377,54 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
         "peak_gbs": hbm_peak, "frac": ub / (us / 1e6) / 1e9 / hbm_peak,
         "peak_kind": f"{peak_kind} hbm copy"}
     del pool, args
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def time_scan(s, **kw):
+        """Average device time of one chunk_scan call on workload s (inputs resident)."""
+        tens = [T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D, s.dt_bias, s.initial_states)]
+        x, dt, A, B, C, Dp, bias, init = tens
+        hi = torch.from_numpy(s.has_initial_state).to(dev)
+        cu = torch.from_numpy(s.cu_seqlens).to(dev)
+        y = torch.empty_like(x)
+        fs = torch.empty((s.nseq, s.H, s.P, s.N), dtype=torch.float32, device=dev)
+        nws = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu, chunk_size=s.chunk_size,
+                                            seg_chunks=kw.get("seg_chunks", 0))
+        ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+
+        def run():
+            ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp,
+                           dt_bias=bias, initial_states=init, has_initial_state=hi, y=y,
+                           final_states=fs, workspace=ws, **kw)
+
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / iters, nws > 0
+
     # large varlen prefill
     s = I.scan_workload("nemotron_h_varlen")
-    tens = [T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D, s.dt_bias, s.initial_states)]
-    x, dt, A, B, C, Dp, bias, init = tens
-    hi = torch.from_numpy(s.has_initial_state).to(dev)
-    cu = torch.from_numpy(s.cu_seqlens).to(dev)
-    y = torch.empty_like(x)
-    fs = torch.empty((s.nseq, s.H, s.P, s.N), dtype=torch.float32, device=dev)
-
-    def run():
-        ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp, dt_bias=bias,
-                       initial_states=init, has_initial_state=hi, y=y, final_states=fs)
-
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(iters):
-        run()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / iters
+    us, split = time_scan(s)
     sb = scan_bytes(s.T, s.H, s.P, s.G, s.N, s.nseq)
     res["scan_nemotron_h_varlen"] = {
         "workload": "4 packed sequences [8192,3000,517,4675], H=128 P=64 G=8 N=128, chunk 128 "
                     "(inputs 0.6 GB > L2)", "tokens_per_s": s.T / (us / 1e6),
-        "avg_launch_us": us, "algorithmic_bytes_per_launch": sb,
+        "avg_launch_us": us, "split_into_segments": split, "algorithmic_bytes_per_launch": sb,
         "achieved_gbs": sb / (us / 1e6) / 1e9, "frac_hbm": sb / (us / 1e6) / 1e9 / hbm_peak}
+    # one long sequence on few heads: the case sequence splitting is for
+    s = I.scan_workload("mamba2_130m", seqlens=[16384])
+    us, split = time_scan(s)
+    us1, _ = time_scan(s, seg_chunks=-1)
+    sb = scan_bytes(s.T, s.H, s.P, s.G, s.N, s.nseq)
+    res["scan_single_16384"] = {
+        "workload": "one 16384-token sequence, H=24 P=64 G=1 N=128, chunk 256",
+        "tokens_per_s": s.T / (us / 1e6), "avg_launch_us": us, "split_into_segments": split,
+        "unsplit_us": us1, "achieved_gbs": sb / (us / 1e6) / 1e9,
+        "frac_hbm": sb / (us / 1e6) / 1e9 / hbm_peak}
     return res
 
 

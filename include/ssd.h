@@ -18,7 +18,8 @@
  * Conventions shared by every entry point:
  *   - Every pointer argument is DEVICE memory owned by the caller, except the args
  *     structs themselves (host).  The library keeps no pointer after it returns and
- *     allocates no memory: no cudaMalloc, no workspace.
+ *     allocates no memory; the one scratch buffer (the scan's optional workspace) is
+ *     the caller's too.
  *   - Every call is asynchronous on the caller's stream (a cudaStream_t passed as
  *     ssd_stream_t; NULL = the legacy default stream).  Nothing is copied device to
  *     host and no call synchronises, except ssd_read_status.
@@ -106,6 +107,9 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  *   chunk_size: 1 .. 256 (the tensor-core path takes 64, 128 or 256)
  *   impl: SSD_IMPL_*; p_block: 0 = choose, else the channel split of the tensor-core
  *     path (16, 32 or 64; must divide P)
+ *   seg_chunks, workspace, workspace_bytes: sequence splitting of the tensor-core path
+ *     (see ssd_chunk_scan_workspace_size; zeros = run unsplit; -1 <= seg_chunks, and a
+ *     nonzero workspace_bytes needs a workspace pointer, else SSD_ERR_INVALID_ARG)
  *   d_status: uint32 device word or NULL
  * Shapes: H % G == 0; SIMT path N <= 256; tensor-core path bf16, N == 128,
  * P % 16 == 0, 16-byte aligned rows.  Outputs must not alias inputs.
@@ -133,9 +137,33 @@ typedef struct {
   uint32_t* d_status;
   int32_t impl;
   int32_t p_block;
+  int32_t seg_chunks;
+  void* workspace;
+  size_t workspace_bytes;
 } ssd_scan_args;
 
 SSD_API ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_chunk_scan_workspace_size -- device workspace (bytes) the tensor-core scan wants
+ * for these arguments; 0 when it will not split sequences.
+ *
+ * The tensor-core path may split a sequence into segments of seg_chunks 128-token chunks
+ * so that more chains run in parallel: each segment is scanned from a zero state, the
+ * segment end states are chained afterwards (h_in(k+1) = exp(sum of dt A over segment k)
+ * h_in(k) + local end state of k), and y of every later segment receives the
+ * exp(cumulative decay) C h_in^T term it was missing.  The result is the same chunked
+ * evaluation of the recurrence, regrouped.  The workspace holds one fp32 [H, P, N] state
+ * per segment and one fp32 decay per token and head; it is caller-owned device memory of at least the returned size, 256-byte
+ * aligned, passed in args->workspace / workspace_bytes, and its contents need not be
+ * initialised.  With no or too small a workspace and seg_chunks = 0 the scan runs
+ * without splitting.  A sequence has at most 64 segments (a longer segment length is
+ * used where seg_chunks would give more).
+ *   seg_chunks: 0 = choose (needs the workspace); -1 = never split; k >= 1 = split into
+ *   segments of k chunks (SSD_ERR_INVALID_ARG if the workspace is missing or too small).
+ * Fills nothing else; never synchronises.
+ * ------------------------------------------------------------------------------------ */
+SSD_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args);
 
 /* ------------------------------------------------------------------------------------
  * ssd_state_update -- one decode token per request on a pooled state cache,

@@ -44,13 +44,22 @@
 // per element instead of an exponential.  The decay warp checks, per block, that both
 // factors stay at most 2^64; a block that fails takes the exact per-element exponential.
 //
+// Few long sequences leave most SMs idle (a chain is one CTA).  The planner may then cut
+// each sequence into segments of segc chunks, every segment its own chain started from a
+// zero state that leaves its local end state in a caller-provided workspace.  A small
+// tensor-core fix-up kernel, launched to overlap this kernel's tail, then chains those
+// end states into the state each later segment entered with, adds that state's
+// contribution to the segment's outputs and writes the final states.
+//
 // The chunk is the 128-row tcgen05 tile: sequences are split into 128-token chunks
 // starting at their first token.  Chunked evaluation is exact for any chunk length, so
 // the result equals the requested chunk_size's up to rounding.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
+#include "scan_segments.cuh"
 #include "ssd_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -98,7 +107,9 @@ struct TcParams {
   __nv_bfloat16* y;
   float* fin;
   uint32_t* status;
-  int nseq, T, H, P, G, npb, dt_softplus;
+  float* ws_h;    // split sequences: local end state per segment [nseg, H, P, N]
+  float* ws_cs;   // split sequences: log2 decay from the segment start to each token [T, H]
+  int nseq, T, H, P, G, npb, dt_softplus, segc;
 };
 
 template <int PB>
@@ -135,7 +146,7 @@ __device__ __forceinline__ float softplus_fast(float v) {
   return v < -8.f ? e : __logf(1.f + e);
 }
 
-template <int PB>
+template <int PB, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams prm) {
@@ -148,11 +159,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit = blockIdx.x;
   const int pbk = unit % prm.npb;
   const int h = (unit / prm.npb) % prm.H;
-  const int s = unit / (prm.npb * prm.H);
+  const int j = unit / (prm.npb * prm.H);  // the sequence, or the segment when split
   const int p0 = pbk * PB;
   const int H = prm.H, P = prm.P;
   const int g = h / (H / prm.G);
 
+  int s = j, kseg = 0, nseg_s = 1;
+  if constexpr (kSplit) {  // a separate instance: the plain chain carries none of this
+    __shared__ int seg_info[3];
+    if (threadIdx.x == 0) {
+      int ss = -1, kk = 0, nn = 0;
+      find_segment(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn);
+      seg_info[0] = ss;
+      seg_info[1] = kk;
+      seg_info[2] = nn;
+    }
+    __syncthreads();
+    s = seg_info[0];
+    kseg = seg_info[1];
+    nseg_s = seg_info[2];
+    if (s < 0) return;  // past the batch's last segment
+  }
   if (unit == 0 && threadIdx.x == 0 && (prm.cu[0] != 0 || prm.cu[prm.nseq] != prm.T))
     set_status(prm.status, SSD_DEV_SEQ_META);
   const int t0 = prm.cu[s], t1 = prm.cu[s + 1];
@@ -162,16 +189,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const float Ah = prm.A[h];
   const size_t PN = (size_t)P * NSTATE;
-  float* fin = prm.fin ? prm.fin + ((size_t)s * H + h) * PN + (size_t)p0 * NSTATE : nullptr;
+  // this CTA's chunks: [c0, c0 + nch) of the sequence, first token tb
+  const int nch_s = (t1 - t0 + QT - 1) / QT;
+  const int c0 = kSplit ? kseg * prm.segc : 0;
+  const int nch = kSplit ? max(0, min(prm.segc, nch_s - c0)) : nch_s;
+  const int tb = t0 + c0 * QT;
+  const int te = min(t1, tb + nch * QT);
+  const bool split = nseg_s > 1;
+  // where this CTA's end state goes: the final state, or (split) the segment's local one
+  auto end_state = [&]() -> float* {
+    if (split) return prm.ws_h + ((size_t)j * H + h) * PN + (size_t)p0 * NSTATE;
+    return prm.fin ? prm.fin + ((size_t)s * H + h) * PN + (size_t)p0 * NSTATE : nullptr;
+  };
   if (!(Ah < 0.f)) {  // sign test (NaN, +0, -0 fail): the chain produces zeros
-    if (threadIdx.x == 0 && pbk == 0) set_status(prm.status, SSD_DEV_A_NOT_NEG);
-    for (int e = threadIdx.x; e < (t1 - t0) * PB; e += kThreads)
-      prm.y[((size_t)(t0 + e / PB) * H + h) * P + p0 + e % PB] = __float2bfloat16_rn(0.f);
+    if (threadIdx.x == 0 && pbk == 0 && kseg == 0) set_status(prm.status, SSD_DEV_A_NOT_NEG);
+    for (int e = threadIdx.x; e < (te - tb) * PB; e += kThreads)
+      prm.y[((size_t)(tb + e / PB) * H + h) * P + p0 + e % PB] = __float2bfloat16_rn(0.f);
+    // the first segment zeroes the final state (the fix-up kernel skips such heads)
+    float* fin = (prm.fin && kseg == 0)
+                     ? prm.fin + ((size_t)s * H + h) * PN + (size_t)p0 * NSTATE
+                     : nullptr;
     if (fin)
       for (int e = threadIdx.x; e < PB * NSTATE; e += kThreads) fin[e] = 0.f;
     return;
   }
-  const int nch = (t1 - t0 + QT - 1) / QT;
 
   float* pro = reinterpret_cast<float*>(sm + L::kPro);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
@@ -247,6 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the fix-up kernel (split sequences) may be scheduled once every CTA holds its tensor
+  // memory; it waits for this grid to complete before it reads what this grid writes
+  if (kSplit && threadIdx.x == 0) griddep_launch_dependents();
   auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
     return warp_wait(bar, par, abort_flag, kWaitLimit);
   };
@@ -256,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr int kAhead = 4;  // L2 prefetch distance, in chunks
       auto prefetch = [&](int c) {
-        const int tok = t0 + c * QT;
+        const int tok = tb + c * QT;
         tma_prefetch_3d(&tmB, 0, g, tok);
         tma_prefetch_3d(&tmB, 64, g, tok);
         tma_prefetch_3d(&tmC, 0, g, tok);
@@ -266,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kAhead && c < nch; ++c) prefetch(c);
       int nb_iss = 0, nc_iss = 0, nx_iss = 0;
       for (int c = 0; c < nch; ++c) {
-        const int tok = t0 + c * QT;
+        const int tok = tb + c * QT;
         if (c + kAhead < nch) prefetch(c + kAhead);
         const int sb = c % NBB, sc = c % NBC, sx = c % NX;
         if (c >= NBB && !mbar_wait(&b_empty[sb], ((c / NBB) - 1) & 1, abort_flag, kWaitLimit))
@@ -306,11 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_dt = [&](int c) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int tok = t0 + c * QT + 32 * k + lane;
+        const int tok = tb + c * QT + 32 * k + lane;
         dt_raw[k] = tok < t1 ? prm.dt[(size_t)tok * H + h] : 0.f;
       }
     };
     if (nch > 0) load_dt(0);
+    // split sequences: each token's log2 decay from its segment start, for the fix-up
+    float* cs_out = (kSplit && split && pbk == 0) ? prm.ws_cs + h : nullptr;
+    float seg_off = 0.f;
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB;
       if (c >= NB && !wwait(&pro_empty[b], ((c / NB) - 1) & 1)) break;
@@ -319,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float d[4], cs[4], carry = 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int tok = t0 + c * QT + 32 * k + lane;
+        const int tok = tb + c * QT + 32 * k + lane;
         const float v0 = dt_raw[k] + bias;
         d[k] = tok < t1 ? (prm.dt_softplus ? softplus_fast(v0) : v0) : 0.f;
         float v = d[k] * a2;
@@ -333,6 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (c + 1 < nch) load_dt(c + 1);
       const float cs_last = carry;
+      if (kSplit && cs_out) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tok = tb + c * QT + 32 * k + lane;
+          if (tok < t1) cs_out[(size_t)tok * H] = seg_off + cs[k];
+        }
+        seg_off += cs_last;
+      }
       float* pb = pro + b * kProStride;
       float run_max = -INFINITY;  // max of cs over blocks >= k (row-factor bound)
       float blk_max[4];
@@ -346,16 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int j = 32 * k + lane;
+        const int col = 32 * k + lane;
         const float anchor = __shfl_sync(0xffffffffu, cs[k], 0);
         float span = anchor - cs[k];  // column factor exponent
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
           span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, off));
-        pb[kProCs + j] = cs[k];
-        pb[kProDt + j] = d[k];
-        pb[kProColf + j] = ex2(anchor - cs[k]) * d[k];
-        pb[kProW + j] = ex2(cs_last - cs[k]) * d[k];
+        pb[kProCs + col] = cs[k];
+        pb[kProDt + col] = d[k];
+        pb[kProColf + col] = ex2(anchor - cs[k]) * d[k];
+        pb[kProW + col] = ex2(cs_last - cs[k]) * d[k];
         if (lane == 0)
           pb[kProSafe + k] = (span <= kFactorLimit && blk_max[k] - anchor <= kFactorLimit) ? 1.f : 0.f;
       }
@@ -575,7 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * q + lane;           // token row i of y, state row n of h
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
     float hreg[PB];                        // h[n = r][p0 + k]
-    const bool has_init = prm.init && (prm.has_init == nullptr || prm.has_init[s] != 0);
+    const bool has_init =
+        kseg == 0 && prm.init && (prm.has_init == nullptr || prm.has_init[s] != 0);
 #pragma unroll
     for (int k = 0; k < PB; ++k)
       hreg[k] = has_init ? prm.init[((size_t)s * H + h) * PN + (size_t)(p0 + k) * NSTATE + r] : 0.f;
@@ -626,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (warp == 2 + kMaskWarps) TRACE(c, 13);
       const float e_i = ex2(pb[kProCs + r]);
-      const int tok = t0 + c * QT + r;
+      const int tok = tb + c * QT + r;
       __nv_bfloat16* yrow = prm.y + ((size_t)tok * H + h) * P + p0;
       const uint8_t* xt = sm + L::kX + sx * L::kXPad;
       const uint32_t colY = tmem + lrow + L::kY0 + (c & 1) * PB;
@@ -661,9 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (warp == 2 + kMaskWarps) TRACE(c, 8);
     }
-    if (ok && fin) {
+    // the final state, or a segment's local end state (the fix-up kernel chains those)
+    float* hout = ok ? end_state() : nullptr;
+    if (hout) {
 #pragma unroll
-      for (int k = 0; k < PB; ++k) fin[(size_t)k * NSTATE + r] = hreg[k];
+      for (int k = 0; k < PB; ++k) hout[(size_t)k * NSTATE + r] = hreg[k];
     }
   }
 
@@ -682,6 +740,298 @@ extern "C" SSD_API int ssd_trace_read(long long* dst) {
 }
 namespace {
 #endif
+
+// ------------------------------------------------------------------ split sequences
+//
+// When a sequence is split into segments, segment k > 0 was scanned from a zero state and
+// left its local end state L_k.  With d_k the segment's total log2 decay, the state that
+// entered segment k is
+//     H_1 = L_0,   H_{i+1} = 2^{d_i} H_i + L_i,
+// the final state is 2^{d_last} H_last + L_last, and the outputs of segment k miss
+//     y_t += 2^{cs'_t} C_t H_k^T,   cs'_t = sum of dt A log2(e) from the segment start to t.
+// The scan kernel leaves L_k and every token's cs'_t (d_k is cs' at the segment's last
+// token) in the workspace.  One fix-up CTA per (later segment, head, channel block) forms
+// H_k from the L_i, adds that term chunk by chunk (tensor core: C H_k^T) and, for the
+// last segment, writes the final state.  It is launched with programmatic stream
+// serialisation: its set-up and its C loads overlap the scan kernel's tail, and it waits
+// for the scan to complete before it reads what the scan wrote.
+
+#ifdef SSD_TRACE
+__device__ long long g_trace_fix[32][4];
+#define TRACE_FIX(i, slot, unit_id)                                                   \
+  do {                                                                                \
+    if (blockIdx.x == (unit_id) && (i) < 32) g_trace_fix[(i)][(slot)] = clock64();    \
+  } while (0)
+}  // namespace
+extern "C" SSD_API int ssd_trace_fix_read(long long* dst) {
+  return (int)cudaMemcpyFromSymbol(dst, g_trace_fix, sizeof(g_trace_fix));
+}
+namespace {
+#else
+#define TRACE_FIX(i, slot, unit_id) do { } while (0)
+#endif
+
+constexpr int kMaxSegs = 64;      // segments per sequence (the planner keeps to it)
+constexpr int kFixThreads = 192;  // warp 0 TMA, warp 1 TMEM + MMA, warps 2-5 epilogue
+
+struct FixParams {
+  const float* A;
+  const int32_t* cu;
+  __nv_bfloat16* y;
+  const float* ws_h;   // local end states of the segments [nseg, H, P, N]
+  const float* ws_cs;  // log2 decay from the segment start to each token [T, H]
+  float* fin;
+  uint32_t* status;
+  int nseq, T, H, P, G, npb, segc;
+};
+
+template <int PB>
+struct FixLayout {
+  static constexpr int kXRow = PB * 2;
+  static constexpr int kC = 0;                          // 2 x C tile (32 KB each)
+  static constexpr int kHT = 65536;                     // H_k^T, [N rows][PB] bf16
+  static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
+  static constexpr int kBar = kHT + kHTPad;
+  static constexpr int kNumBar = 10;
+  static constexpr int kFlags = kBar + kNumBar * 8;
+  static constexpr int kSmemBytes = kFlags + 16 + 1024;
+  static constexpr int kSwB = PB == 64 ? 3 : PB == 32 ? 2 : 1;
+  static constexpr uint32_t kSwCode = PB == 64 ? kSw128 : PB == 32 ? kSw64 : kSw32;
+  static_assert(kBar % 8 == 0, "mbarriers need 8-byte alignment");
+};
+
+template <int PB>
+__global__ void __launch_bounds__(kFixThreads, 2)
+    scan_fixup_kernel(const __grid_constant__ CUtensorMap tmC, const FixParams prm) {
+  using L = FixLayout<PB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x;
+  const int pbk = unit % prm.npb;
+  const int h = (unit / prm.npb) % prm.H;
+  const int j = unit / (prm.npb * prm.H);
+  const int p0 = pbk * PB;
+  const int H = prm.H, P = prm.P;
+  __shared__ int seg_info[3];
+  const int tr_unit = 2 * prm.H * prm.npb;  // the CTA a trace build records
+  (void)tr_unit;
+  if (threadIdx.x == 0) TRACE_FIX(0, 0, tr_unit);
+  if (threadIdx.x == 0) {
+    int ss = -1, kk = 0, nn = 0;
+    find_segment(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn);
+    seg_info[0] = ss;
+    seg_info[1] = kk;
+    seg_info[2] = nn;
+  }
+  __syncthreads();
+  const int s = seg_info[0], kseg = seg_info[1], nseg_s = seg_info[2];
+  if (s < 0 || kseg == 0) return;  // a first segment has nothing to add
+  const int t0 = prm.cu[s], t1 = prm.cu[s + 1];
+  if (!(0 <= t0 && t0 <= t1 && t1 <= prm.T)) return;  // reported by the scan kernel
+  const float Ah = prm.A[h];
+  if (!(Ah < 0.f)) return;  // the scan kernel zeroed that head
+  if (nseg_s > kMaxSegs) {  // the planner never gets here; a malformed batch might
+    if (threadIdx.x == 0) set_status(prm.status, SSD_DEV_SEQ_META);
+    return;
+  }
+  const int seg_tokens = prm.segc * QT;
+  const int nch_s = (t1 - t0 + QT - 1) / QT;
+  const int c0 = kseg * prm.segc;
+  const int nch = max(0, min(prm.segc, nch_s - c0));
+  const int tb = t0 + c0 * QT;
+  const bool last = kseg == nseg_s - 1;
+  const int gidx = h / (H / prm.G);
+  const size_t PN = (size_t)P * NSTATE;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint64_t* c_full = bars;         // [2] C landed
+  uint64_t* c_empty = bars + 2;    // [2] C read by the tensor core
+  uint64_t* acc_full = bars + 4;   // [2] C H_k^T of a chunk in TMEM
+  uint64_t* acc_empty = bars + 6;  // [2] read by the 4 epilogue warps
+  uint64_t* h_ready = bars + 8;    //     H_k^T in shared memory
+  uint64_t* drain = bars + 9;      //     teardown: all MMAs retired
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c_full[i], 1);
+      mbar_init(&c_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    mbar_init(h_ready, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
+    return warp_wait(bar, par, abort_flag, kWaitLimit);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer: C of every chunk
+    if (lane == 0) {
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        if (c >= 2 && !mbar_wait(&c_empty[st], ((c >> 1) - 1) & 1, abort_flag, kWaitLimit)) break;
+        uint8_t* ct = sm + L::kC + st * 32768;
+        mbar_arrive_expect_tx(&c_full[st], 32768);
+        tma_load_3d(ct, &tmC, &c_full[st], 0, gidx, tb + c * QT);
+        tma_load_3d(ct + 16384, &tmC, &c_full[st], 64, gidx, tb + c * QT);
+        TRACE_FIX(1 + c, 3, tr_unit);
+        issued = c + 1;
+      }
+      for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
+        mbar_wait_drain(&c_full[c & 1], (c >> 1) & 1, kWaitLimit);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer: Yfix = C H_k^T
+    if (lane == 0) {
+      constexpr uint32_t idO = make_idesc_bf16(128, PB, false, true);
+      const uint64_t dC0 = make_sdesc(smem_u32(sm + L::kC), 16, 1024, kSw128);
+      const uint64_t dH = make_sdesc(smem_u32(sm + L::kHT), L::kHTPad, 8 * L::kXRow, L::kSwCode);
+      bool ok = mbar_wait(h_ready, 0, abort_flag, kWaitLimit);
+      for (int c = 0; ok && c < nch; ++c) {
+        const int st = c & 1;
+        if (!(ok = mbar_wait(&c_full[st], (c >> 1) & 1, abort_flag, kWaitLimit))) break;
+        if (c >= 2 && !(ok = mbar_wait(&acc_empty[st], ((c >> 1) - 1) & 1, abort_flag, kWaitLimit)))
+          break;
+        tc_fence_after();
+        const uint64_t da = dC0 + (uint64_t)(st * (32768 >> 4));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // K = N = 128 in steps of 16
+          const uint64_t ko = (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4));
+          mma_ss(tmem + st * PB, da + ko, dH + kk * L::kXRow, idO, kk > 0);
+        }
+        mma_commit(&acc_full[st]);
+        mma_commit(&c_empty[st]);
+      }
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, kWaitLimit);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps (one per TMEM quadrant)
+    const int q = warp & 3;
+    const int r = 32 * q + lane;  // state row n of H_k^T, token row of a chunk
+    const uint32_t lrow = (uint32_t)(32 * q) << 16;
+    // everything below reads what the scan kernel wrote
+    griddep_wait();
+    if (r == 0) TRACE_FIX(0, 2, tr_unit);
+    // d_i: the decay from segment i's start to its last token, as the scan kernel left it
+    auto seg_decay = [&](int i) -> float {
+      const int te = min(t1, t0 + (i + 1) * seg_tokens);
+      return prm.ws_cs[(size_t)(te - 1) * H + h];
+    };
+    // 1. H_k from the local end states: H_1 = L_0, H_{i+1} = 2^{d_i} H_i + L_i
+    const float* loc0 = prm.ws_h + ((size_t)(j - kseg) * H + h) * PN + (size_t)p0 * NSTATE + r;
+    float hin[PB];
+#pragma unroll
+    for (int k = 0; k < PB; ++k) hin[k] = loc0[(size_t)k * NSTATE];
+    for (int i = 1; i < kseg; ++i) {
+      const float d = ex2(seg_decay(i));
+      const float* li = loc0 + (size_t)i * H * PN;
+#pragma unroll
+      for (int k = 0; k < PB; ++k) hin[k] = fmaf(d, hin[k], li[(size_t)k * NSTATE]);
+    }
+    {
+      uint8_t* ht = sm + L::kHT;
+#pragma unroll
+      for (int k8 = 0; k8 < PB / 8; ++k8) {
+        uint4 w;
+        w.x = pack_bf16(hin[8 * k8 + 0], hin[8 * k8 + 1]);
+        w.y = pack_bf16(hin[8 * k8 + 2], hin[8 * k8 + 3]);
+        w.z = pack_bf16(hin[8 * k8 + 4], hin[8 * k8 + 5]);
+        w.w = pack_bf16(hin[8 * k8 + 6], hin[8 * k8 + 7]);
+        *reinterpret_cast<uint4*>(ht + swz((uint32_t)(r * L::kXRow + 16 * k8), L::kSwB)) = w;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(h_ready);
+    }
+    if (r == 0) TRACE_FIX(0, 3, tr_unit);
+    if (last && prm.fin) {  // final state = 2^{d_last} H_last + L_last
+      const float d = ex2(seg_decay(kseg));
+      const float* ll = loc0 + (size_t)kseg * H * PN;
+      // every load first: a store between them could alias the next load and would
+      // serialise the whole row on memory latency
+#pragma unroll
+      for (int k = 0; k < PB; ++k) hin[k] = fmaf(d, hin[k], ll[(size_t)k * NSTATE]);
+      float* f = prm.fin + ((size_t)s * H + h) * PN + (size_t)p0 * NSTATE + r;
+#pragma unroll
+      for (int k = 0; k < PB; ++k) f[(size_t)k * NSTATE] = hin[k];
+    }
+    // 2. per chunk: y += 2^{cs'} Yfix, cs' the decay from the segment start to the row's
+    // token.  Row loads run two chunks ahead (two register sets), so a chunk waits on
+    // memory only if the tensor core is faster than two loads in flight.
+    uint4 ya[PB / 8], yb[PB / 8];
+    float csa = 0.f, csb = 0.f;
+    auto load_row = [&](int c, uint4 (&yr)[PB / 8], float& cv) {
+      const int tok = tb + c * QT + r;
+      if (tok < t1) {
+        const uint4* src = reinterpret_cast<const uint4*>(prm.y + ((size_t)tok * H + h) * P + p0);
+#pragma unroll
+        for (int e = 0; e < PB / 8; ++e) yr[e] = src[e];
+        cv = prm.ws_cs[(size_t)tok * H + h];
+      }
+    };
+    auto process = [&](int c, uint4 (&yr)[PB / 8], float cv) -> bool {
+      const int st = c & 1;
+      const int tok = tb + c * QT + r;
+      if (r == 0) TRACE_FIX(1 + c, 0, tr_unit);
+      if (!wwait(&acc_full[st], (c >> 1) & 1)) return false;
+      if (r == 0) TRACE_FIX(1 + c, 1, tr_unit);
+      tc_fence_after();
+      const float scale = ex2(cv);
+#pragma unroll
+      for (int sl = 0; sl < PB / 16; ++sl) {
+        float fv[16];
+        tmem_ld16(tmem + lrow + st * PB + 16 * sl, fv);
+        __nv_bfloat162* y2 = reinterpret_cast<__nv_bfloat162*>(&yr[2 * sl]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 yf = __bfloat1622float2(y2[e]);
+          y2[e] = __floats2bfloat162_rn(fmaf(scale, fv[2 * e], yf.x),
+                                        fmaf(scale, fv[2 * e + 1], yf.y));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[st]);
+      if (tok < t1) {
+        uint4* dst = reinterpret_cast<uint4*>(prm.y + ((size_t)tok * H + h) * P + p0);
+#pragma unroll
+        for (int e = 0; e < PB / 8; ++e) dst[e] = yr[e];
+      }
+      if (r == 0) TRACE_FIX(1 + c, 2, tr_unit);
+      return true;
+    };
+    if (nch > 0) load_row(0, ya, csa);
+    if (nch > 1) load_row(1, yb, csb);
+    for (int c = 0; c < nch; c += 2) {
+      if (!process(c, ya, csa)) break;
+      if (c + 2 < nch) load_row(c + 2, ya, csa);
+      if (c + 1 >= nch) break;
+      if (!process(c + 1, yb, csb)) break;
+      if (c + 3 < nch) load_row(c + 3, yb, csb);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+  if (threadIdx.x == 0 && *abort_flag) set_status(prm.status, SSD_DEV_TIMEOUT);
+}
 
 // ------------------------------------------------------------------ host side
 
@@ -713,8 +1063,121 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+    else
+      sms = 148;
+  }
+  return sms;
+}
+
+// How one call runs: channel block PB, segment length segc (0 = sequences are not split),
+// the segment count the grid covers and the workspace that needs.
+struct ScanPlan {
+  int pb = 0;
+  int segc = 0;
+  long long nseg = 0;
+  size_t ws_bytes = 0;
+};
+
+// Upper bound of the segment count of a batch of nseq sequences and T tokens:
+// max(1, ceil(nch_s / segc)) <= 1 + nch_s / segc and sum nch_s <= (T + 127 nseq) / 128.
+long long seg_capacity(const ssd_scan_args& a, int segc) {
+  return (long long)a.nseq + ((long long)a.T + (long long)(kScanChunk - 1) * a.nseq) /
+                                 ((long long)kScanChunk * segc);
+}
+
+// Workspace of a split: the segments' local end states [nseg, H, P, N] fp32 (a multiple
+// of 512 bytes), then each token's decay from its segment start [T, H] fp32.
+size_t ws_states_bytes(const ssd_scan_args& a, long long nseg) {
+  return (size_t)nseg * a.H * a.P * NSTATE * sizeof(float);
+}
+size_t ws_bytes_for(const ssd_scan_args& a, long long nseg) {
+  const size_t cs = (size_t)a.T * a.H * sizeof(float);
+  return (ws_states_bytes(a, nseg) + cs + 255) / 256 * 256;
+}
+
+// Smallest segment length that keeps every sequence within kMaxSegs segments: no
+// sequence has more than ceil(T / 128) chunks.
+int min_segc(const ssd_scan_args& a) {
+  const long long nch_max = ((long long)a.T + kScanChunk - 1) / kScanChunk;
+  return (int)std::max<long long>(1, (nch_max + kMaxSegs - 1) / kMaxSegs);
+}
+
+// Cost model in units of one 128-token chunk of a 64-channel CTA in its steady state
+// (about 2 us), fitted to measured times of the 2 x 2048-token and 4-sequence varlen
+// batches and of single 16K-token sequences.  The host sees only T and nseq (the
+// lengths live on the device), so sequences are taken as equally long.  One CTA per SM;
+// a CTA of channel block PB that runs n chunks costs about kRamp + n (1 + PB/256) (the
+// mask and C.B^T work does not shrink with PB; kRamp is the pipeline fill of its first
+// chunk).  A split adds the fix-up grid over the later segments, two CTAs per SM: its
+// set-up, one chained step per segment before it (the entering state) and a per-chunk
+// cost close to the scan's own.
+constexpr double kRamp = 3.0, kFixBase = 4.0, kFixPerSeg = 1.0, kFixPerChunk = 1.5;
+
+double plan_cost(const ssd_scan_args& a, int pb, int segc) {
+  const int sms = sm_count();
+  const long long per = ((long long)a.T + a.nseq - 1) / a.nseq;
+  const long long nch = std::max<long long>(1, (per + kScanChunk - 1) / kScanChunk);
+  const long long nseg = segc > 0 ? (nch + segc - 1) / segc : 1;
+  const long long chain = segc > 0 ? std::min<long long>(segc, nch) : nch;
+  const long long per_seg = (long long)a.H * (a.P / pb);
+  const long long ctas = (long long)a.nseq * nseg * per_seg;
+  const long long waves = (ctas + sms - 1) / sms;
+  double cost = (double)waves * (kRamp + chain * (1.0 + pb / 256.0));
+  if (nseg > 1) {
+    const long long fix_ctas = (long long)a.nseq * (nseg - 1) * per_seg;
+    const long long fix_waves = (fix_ctas + 2 * sms - 1) / (2 * sms);
+    cost += fix_waves * (kFixBase + kFixPerSeg * nseg + kFixPerChunk * chain);
+  }
+  return cost;
+}
+
+constexpr int kMaxSplitSeqs = 1024;  // each CTA walks the sequence table to find its segment
+
+bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out) {
+  ScanPlan best;
+  double best_cost = 1e300;
+  const long long per = ((long long)a.T + a.nseq - 1) / a.nseq;
+  const int nch = (int)std::max<long long>(1, (per + kScanChunk - 1) / kScanChunk);
+  const int lo = min_segc(a);
+  for (int pb : {64, 32, 16}) {
+    if (a.P % pb || (a.p_block && a.p_block != pb)) continue;
+    auto consider = [&](int segc) {
+      const double c = plan_cost(a, pb, segc);
+      if (c < best_cost - 1e-9) {
+        best_cost = c;
+        best.pb = pb;
+        best.segc = segc;
+      }
+    };
+    if (a.seg_chunks >= 1) {
+      consider(std::max(a.seg_chunks, lo));
+    } else {
+      consider(0);
+      if (allow_split && a.seg_chunks == 0 && a.nseq <= kMaxSplitSeqs)
+        for (int segc = lo; segc < nch; ++segc) consider(segc);
+    }
+  }
+  if (best.pb == 0) return false;
+  if (best.segc > 0) {
+    best.nseg = seg_capacity(a, best.segc);
+    best.ws_bytes = ws_bytes_for(a, best.nseg);
+  } else {
+    best.nseg = a.nseq;
+  }
+  if (best.nseg * a.H * (a.P / best.pb) > 0x7fffffffLL) return false;
+  *out = best;
+  return true;
+}
+
 template <int PB>
-ssd_status launch_pb(const ssd_scan_args& a, cudaStream_t st) {
+ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t st) {
   using L = Layout<PB>;
   const int64_t xs = a.x_stride_t ? a.x_stride_t : (int64_t)a.H * a.P;
   const int64_t bs = a.B_stride_t ? a.B_stride_t : (int64_t)a.G * a.N;
@@ -732,11 +1195,20 @@ ssd_status launch_pb(const ssd_scan_args& a, cudaStream_t st) {
     return SSD_ERR_CUDA;
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
-    if (cudaFuncSetAttribute(scan_tc_kernel<PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(scan_tc_kernel<PB, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(scan_tc_kernel<PB, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(scan_fixup_kernel<PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FixLayout<PB>::kSmemBytes) != cudaSuccess)
       return SSD_ERR_CUDA;
     attr_set = true;
   }
+  const bool split = plan.segc > 0;
+  float* ws_h = split ? static_cast<float*>(a.workspace) : nullptr;
+  float* ws_cs = split ? ws_h + ws_states_bytes(a, plan.nseg) / sizeof(float) : nullptr;
   TcParams prm;
   prm.dt = a.dt;
   prm.dt_bias = a.dt_bias;
@@ -748,6 +1220,8 @@ ssd_status launch_pb(const ssd_scan_args& a, cudaStream_t st) {
   prm.y = static_cast<__nv_bfloat16*>(a.y);
   prm.fin = a.final_states;
   prm.status = a.d_status;
+  prm.ws_h = ws_h;
+  prm.ws_cs = ws_cs;
   prm.nseq = a.nseq;
   prm.T = a.T;
   prm.H = a.H;
@@ -755,14 +1229,48 @@ ssd_status launch_pb(const ssd_scan_args& a, cudaStream_t st) {
   prm.G = a.G;
   prm.npb = a.P / PB;
   prm.dt_softplus = a.dt_softplus;
-  const long long grid = (long long)a.nseq * a.H * prm.npb;
-  scan_tc_kernel<PB><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
+  prm.segc = plan.segc;
+  const long long grid = plan.nseg * a.H * prm.npb;
+  if (!split) {
+    scan_tc_kernel<PB, false><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
+  scan_tc_kernel<PB, true><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
+  if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+  FixParams fp;
+  fp.A = a.A;
+  fp.cu = a.cu_seqlens;
+  fp.y = prm.y;
+  fp.ws_h = ws_h;
+  fp.ws_cs = ws_cs;
+  fp.fin = a.final_states;
+  fp.status = a.d_status;
+  fp.nseq = a.nseq;
+  fp.T = a.T;
+  fp.H = a.H;
+  fp.P = a.P;
+  fp.G = a.G;
+  fp.npb = prm.npb;
+  fp.segc = plan.segc;
+  // programmatic stream serialisation: the fix-up grid may start while the scan grid
+  // drains; it waits for the scan's completion before it reads the scan's outputs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kFixThreads);
+  cfg.dynamicSmemBytes = FixLayout<PB>::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, scan_fixup_kernel<PB>, mC, fp) != cudaSuccess) return SSD_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 }  // namespace
 
-bool scan_tc_supported(const ssd_scan_args& a, int* pb_out) {
+bool scan_tc_supported(const ssd_scan_args& a) {
   if (a.act_dtype != SSD_BF16 || a.N != NSTATE || a.P % 16 != 0 || a.T < 1) return false;
   if (a.chunk_size != 64 && a.chunk_size != 128 && a.chunk_size != 256) return false;
   const int64_t xs = a.x_stride_t ? a.x_stride_t : (int64_t)a.H * a.P;
@@ -771,45 +1279,33 @@ bool scan_tc_supported(const ssd_scan_args& a, int* pb_out) {
   auto al16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
   if (!al16(a.x) || !al16(a.B) || !al16(a.C) || !al16(a.y)) return false;
   if ((xs * 2) % 16 || (bs * 2) % 16 || (cs * 2) % 16) return false;
-  if ((long long)a.nseq * a.H * (a.P / 16) > 0x7fffffffLL) return false;
-  int pb = a.p_block;
-  if (pb) {
-    if (a.P % pb) return false;
-  } else {
-    // One CTA per SM: fewest waves of CTAs over the SMs wins; a CTA's time per chunk
-    // grows only slowly with its channel block (the mask and C.B^T do not depend on it),
-    // measured roughly as 1 + PB/256.
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0, n = 0;
-      if (cudaGetDevice(&dev) == cudaSuccess &&
-          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-        sms = n;
-      else
-        sms = 148;
-    }
-    double best = 1e30;
-    for (int cand : {64, 32, 16}) {
-      if (a.P % cand) continue;
-      const long long ctas = (long long)a.nseq * a.H * (a.P / cand);
-      const long long waves = (ctas + sms - 1) / sms;
-      const double cost = (double)waves * (1.0 + cand / 256.0);
-      if (cost < best - 1e-9) {
-        best = cost;
-        pb = cand;
-      }
-    }
-  }
-  if (pb != 16 && pb != 32 && pb != 64) return false;
-  *pb_out = pb;
-  return true;
+  if (a.p_block && a.P % a.p_block) return false;
+  ScanPlan plan;
+  return plan_scan(a, false, &plan);
 }
 
-ssd_status launch_scan_tc(const ssd_scan_args& a, int pb, cudaStream_t st) {
-  switch (pb) {
-    case 64: return launch_pb<64>(a, st);
-    case 32: return launch_pb<32>(a, st);
-    case 16: return launch_pb<16>(a, st);
+size_t scan_tc_workspace_size(const ssd_scan_args& a) {
+  if (!scan_tc_supported(a) || a.seg_chunks < 0) return 0;
+  ScanPlan plan;
+  if (!plan_scan(a, true, &plan)) return 0;
+  return plan.ws_bytes;
+}
+
+ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t st) {
+  ScanPlan plan;
+  if (!plan_scan(a, a.seg_chunks >= 0, &plan)) return SSD_ERR_UNSUPPORTED;
+  if (plan.segc > 0) {
+    const bool ws_ok = a.workspace && ((uintptr_t)a.workspace & 255u) == 0 &&
+                       a.workspace_bytes >= plan.ws_bytes;
+    if (!ws_ok) {
+      if (a.seg_chunks >= 1) return SSD_ERR_INVALID_ARG;
+      if (!plan_scan(a, false, &plan)) return SSD_ERR_UNSUPPORTED;  // run unsplit
+    }
+  }
+  switch (plan.pb) {
+    case 64: return launch_pb<64>(a, plan, st);
+    case 32: return launch_pb<32>(a, plan, st);
+    case 16: return launch_pb<16>(a, plan, st);
   }
   return SSD_ERR_UNSUPPORTED;
 }

@@ -26,6 +26,8 @@ ssd_status validate_scan(const ssd_scan_args* a) {
   if (a->impl < SSD_IMPL_AUTO || a->impl > SSD_IMPL_TC) return SSD_ERR_INVALID_ARG;
   if (a->p_block != 0 && a->p_block != 16 && a->p_block != 32 && a->p_block != 64)
     return SSD_ERR_INVALID_ARG;
+  if (a->seg_chunks < -1) return SSD_ERR_INVALID_ARG;
+  if (a->workspace_bytes > 0 && !a->workspace) return SSD_ERR_INVALID_ARG;
   if (a->nseq > 65535 || a->H > 65535) return SSD_ERR_UNSUPPORTED;  // grid limits
   return SSD_OK;
 }
@@ -55,14 +57,20 @@ ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream) {
   if (v != SSD_OK) return v;
   const ssd_scan_args& a = *args;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int pb = 0;
-  const bool tc_ok = scan_tc_supported(a, &pb);
+  const bool tc_ok = scan_tc_supported(a);
   if (a.impl == SSD_IMPL_TC || (a.impl == SSD_IMPL_AUTO && tc_ok)) {
     if (!tc_ok) return SSD_ERR_UNSUPPORTED;
-    return launch_scan_tc(a, pb, st);
+    return launch_scan_tc(a, st);
   }
   if (a.N > 256) return SSD_ERR_UNSUPPORTED;
   return launch_scan_simt(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args) {
+  if (validate_scan(args) != SSD_OK) return 0;
+  const ssd_scan_args& a = *args;
+  if (a.impl == SSD_IMPL_SIMT) return 0;
+  return scan_tc_workspace_size(a);
 }
 
 ssd_status ssd_state_update(const ssd_update_args* args, ssd_stream_t stream) {

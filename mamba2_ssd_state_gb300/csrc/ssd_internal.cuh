@@ -36,8 +36,11 @@ cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, vo
                                  ssd_dtype wt, cudaStream_t s);
 cudaError_t launch_scan_simt(const ssd_scan_args& a, cudaStream_t s);
 
-// Tensor-core scan: returns SSD_ERR_UNSUPPORTED for shapes it cannot take.
-bool scan_tc_supported(const ssd_scan_args& a, int* p_block_out);
-ssd_status launch_scan_tc(const ssd_scan_args& a, int p_block, cudaStream_t s);
+// Tensor-core scan: supported shapes, the workspace its plan wants (0 = no split) and the
+// launch (SSD_ERR_UNSUPPORTED for shapes it cannot take, SSD_ERR_INVALID_ARG for a forced
+// split without a large enough workspace).
+bool scan_tc_supported(const ssd_scan_args& a);
+size_t scan_tc_workspace_size(const ssd_scan_args& a);
+ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s);
 
 }  // namespace ssd

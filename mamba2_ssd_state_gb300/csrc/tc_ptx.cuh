@@ -125,6 +125,18 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// Programmatic dependent launch: a grid launched with programmatic stream serialisation
+// may start before the previous grid on the stream ends.  The previous grid signals that
+// its dependents may be scheduled; a dependent waits, before it reads anything the
+// previous grid writes, until that grid has completed and its writes are visible.
+// Both are no-ops when the launch did not ask for the overlap.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

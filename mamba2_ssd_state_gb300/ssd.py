@@ -42,7 +42,8 @@ class ScanArgs(ctypes.Structure):
                 ("initial_states", _vp), ("has_initial_state", _vp), ("cu_seqlens", _vp),
                 ("nseq", _i32), ("T", _i32), ("H", _i32), ("P", _i32), ("G", _i32),
                 ("N", _i32), ("chunk_size", _i32), ("act_dtype", ctypes.c_int), ("y", _vp),
-                ("final_states", _vp), ("d_status", _vp), ("impl", _i32), ("p_block", _i32)]
+                ("final_states", _vp), ("d_status", _vp), ("impl", _i32), ("p_block", _i32),
+                ("seg_chunks", _i32), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class UpdateArgs(ctypes.Structure):
@@ -66,6 +67,8 @@ def load_library(path: str | None = None):
                                "mamba2_ssd_state_gb300.build.build() (needs nvcc)")
         lib = ctypes.CDLL(path)
         lib.ssd_chunk_scan.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+        lib.ssd_chunk_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs)]
+        lib.ssd_chunk_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssd_state_update.argtypes = [ctypes.POINTER(UpdateArgs), _vp]
         lib.gated_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_float,
                                       ctypes.c_int, ctypes.c_int, _vp]
@@ -140,12 +143,14 @@ def _raise(rc, where):
 def chunk_scan(x, dt, A, B, C, *, cu_seqlens, chunk_size, D=None, dt_bias=None,
                dt_softplus=True, initial_states=None, has_initial_state=None, y=None,
                final_states=None, return_final_states=True, status=None, impl="auto",
-               p_block=0, stream=None):
+               p_block=0, seg_chunks=0, workspace=None, stream=None):
     """Mamba2 chunked SSD scan over packed sequences (see ssd_chunk_scan in ssd.h).
 
     x [T,H,P], B/C [T,G,N] (bf16 or fp32, token stride may exceed the dense size);
     dt [T,H], A/D/dt_bias [H], initial_states [nseq,H,P,N] fp32; cu_seqlens int32
-    [nseq+1] on the device.  Returns (y, final_states)."""
+    [nseq+1] on the device.  seg_chunks: 0 = the library decides whether to split long
+    sequences (it then gets a workspace from torch's allocator unless one is passed),
+    -1 = never, k >= 1 = segments of k 128-token chunks.  Returns (y, final_states)."""
     lib = load_library()
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
@@ -188,8 +193,36 @@ def chunk_scan(x, dt, A, B, C, *, cu_seqlens, chunk_size, D=None, dt_bias=None,
     a.act_dtype = act
     a.y, a.final_states, a.d_status = _ptr(y), _ptr(final_states), _ptr(status)
     a.impl, a.p_block = IMPL[impl], int(p_block)
+    a.seg_chunks = int(seg_chunks)
+    if workspace is None and a.seg_chunks >= 0:
+        nbytes = lib.ssd_chunk_scan_workspace_size(ctypes.byref(a))
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _check(workspace, "workspace", torch.uint8, None, dev)
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
     _raise(lib.ssd_chunk_scan(ctypes.byref(a), _stream(stream)), "ssd_chunk_scan")
     return y, final_states
+
+
+def chunk_scan_workspace_size(x, B, C, *, cu_seqlens, chunk_size, impl="auto", p_block=0,
+                              seg_chunks=0):
+    """Bytes of workspace chunk_scan would want for these shapes (0 = it would not split;
+    ssd_chunk_scan_workspace_size in ssd.h).  y is taken as a dense aligned tensor."""
+    lib = load_library()
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    a = ScanArgs()
+    a.struct_size = ctypes.sizeof(ScanArgs)
+    a.x, a.x_stride_t = _ptr(x), _token_stride(x, "x", H * P)
+    a.B, a.B_stride_t = _ptr(B), _token_stride(B, "B", G * N)
+    a.C, a.C_stride_t = _ptr(C), _token_stride(C, "C", G * N)
+    a.dt = a.A = a.y = a.x
+    a.cu_seqlens = _ptr(cu_seqlens)
+    a.nseq, a.T, a.H, a.P, a.G, a.N = cu_seqlens.shape[0] - 1, T, H, P, G, N
+    a.chunk_size, a.act_dtype = int(chunk_size), _act(x)
+    a.impl, a.p_block, a.seg_chunks = IMPL[impl], int(p_block), int(seg_chunks)
+    return int(lib.ssd_chunk_scan_workspace_size(ctypes.byref(a)))
 
 
 def state_update(state_pool, state_indices, x, dt, A, B, C, *, D=None, dt_bias=None,

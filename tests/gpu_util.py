@@ -15,7 +15,7 @@ def dev(t, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(t.values)).to(device=device, dtype=dtype)
 
 
-def scan_gpu(s, impl="auto", p_block=0, final=True, chunk_size=None, D=True):
+def scan_gpu(s, impl="auto", p_block=0, final=True, chunk_size=None, D=True, seg_chunks=0):
     status = ssd.new_status()
     hi = None if s.has_initial_state is None else torch.from_numpy(s.has_initial_state).cuda()
     y, fs = ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C),
@@ -24,7 +24,7 @@ def scan_gpu(s, impl="auto", p_block=0, final=True, chunk_size=None, D=True):
                            D=dev(s.D) if D else None, dt_bias=dev(s.dt_bias),
                            initial_states=dev(s.initial_states), has_initial_state=hi,
                            return_final_states=final, status=status, impl=impl,
-                           p_block=p_block)
+                           p_block=p_block, seg_chunks=seg_chunks)
     rc, bits = ssd.read_status(status)
     torch.cuda.synchronize()
     yf = y.float().cpu().numpy()

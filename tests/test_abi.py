@@ -21,8 +21,9 @@ def lib():
 
 def test_exports_every_declared_entry_point(lib):
     names = ssd.header_functions()
-    assert set(names) == {"ssd_chunk_scan", "ssd_state_update", "gated_rmsnorm",
-                          "ssd_read_status", "ssd_status_string", "ssd_version"}
+    assert set(names) == {"ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
+                          "ssd_state_update", "gated_rmsnorm", "ssd_read_status",
+                          "ssd_status_string", "ssd_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
@@ -68,11 +69,34 @@ def _scan_args(**kw):
     dict(struct_size=8), dict(A=None), dict(cu_seqlens=None), dict(x=None), dict(nseq=0),
     dict(H=3), dict(G=0), dict(P=0), dict(N=0), dict(chunk_size=0), dict(chunk_size=257),
     dict(act_dtype=7), dict(x_stride_t=10), dict(B_stride_t=5), dict(impl=9), dict(p_block=48),
+    dict(seg_chunks=-2), dict(workspace_bytes=256),
 ])
 def test_scan_rejects_bad_arguments(lib, bad):
     a = _scan_args(**bad)
     assert lib.ssd_chunk_scan(ctypes.byref(a), None) == 1
     assert lib.ssd_chunk_scan(None, None) == 1
+
+
+def test_scan_workspace_size(lib):
+    """Host-side planning only: no kernel runs.  A forced split of k chunks per segment
+    wants room for the bound nseq + (T + 127 nseq) // (128 k) on the segment count, each
+    segment holding one fp32 [H, P, N] state, plus one fp32 decay per token and head."""
+    kw = dict(act_dtype=ssd.SSD_BF16, nseq=2, T=4096, H=24, P=64, G=1, N=128, chunk_size=256)
+    size = lambda **o: lib.ssd_chunk_scan_workspace_size(ctypes.byref(_scan_args(**{**kw, **o})))
+    r256 = lambda b: (b + 255) // 256 * 256
+    nseg = 2 + (4096 + 127 * 2) // (128 * 4)
+    assert size(seg_chunks=4) == r256(nseg * 24 * 64 * 128 * 4 + 4096 * 24 * 4)
+    # at most 64 segments per sequence: 1-chunk segments of a 16384-token batch become 2
+    nseg = 2 + (16384 + 127 * 2) // (128 * 2)
+    assert size(seg_chunks=1, T=16384) == r256(nseg * 24 * 64 * 128 * 4 + 16384 * 24 * 4)
+    assert size(seg_chunks=-1) == 0                       # never split
+    assert size(seg_chunks=4, impl=1) == 0                # SIMT path: no workspace
+    assert size(seg_chunks=4, act_dtype=ssd.SSD_F32) == 0  # not a tensor-core shape
+    # the planner keeps two 2048-token sequences whole, and splits one of 16384 tokens
+    assert size() == 0
+    auto = size(nseq=1, T=16384)
+    assert auto > 0 and auto % 256 == 0
+    assert lib.ssd_chunk_scan_workspace_size(None) == 0
 
 
 def test_update_rejects_bad_arguments(lib):

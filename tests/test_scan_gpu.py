@@ -112,6 +112,60 @@ def test_tc_and_simt_agree():
     check_bf16("tc vs simt final", f1, f2)
 
 
+# Split sequences: segments of k 128-token chunks, each scanned from zero, chained by the
+# combine kernel and corrected by the fix-up kernel.  The lengths give sequences of 1 to
+# 8 chunks with ragged tails, exact chunk multiples, one token and an empty one.
+SEG_SEQS = [700, 129, 1, 0, 300, 1000, 257, 128, 385]
+SEG_INIT = [1, 0, 1, 1, 0, 1, 1, 0, 1]
+
+
+@pytest.mark.parametrize("p_block", [16, 32, 64])
+@pytest.mark.parametrize("seg", [1, 2, 3])
+def test_bf16_segmented_parity(p_block, seg):
+    s = I.make_scan_inputs(SEG_SEQS, H=4, P=64, G=2, N=128, chunk_size=256, act="bf16",
+                           seed=141, init=SEG_INIT)
+    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block, seg_chunks=seg)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16(f"seg={seg} pb={p_block} y", y, yr)
+    check_bf16(f"seg={seg} pb={p_block} final", fs, fr)
+    # the empty sequence still returns its initial state, untouched by the chaining
+    np.testing.assert_array_equal(fs[3], s.initial_states.values[3])
+    # and the split agrees with the unsplit chain
+    y1, f1, _ = scan_gpu(s, impl="tc", p_block=p_block, seg_chunks=-1)
+    check_bf16(f"seg={seg} vs unsplit y", y, y1)
+    check_bf16(f"seg={seg} vs unsplit final", fs, f1)
+
+
+def test_segmented_A_not_negative():
+    s = I.make_scan_inputs([600, 200], H=3, P=32, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=143, init="all")
+    A = s.A.values.copy()
+    A[1] = 0.0
+    s.A = I.Tensor(A, "f32")
+    y, fs, bits = scan_gpu(s, impl="tc", seg_chunks=1)
+    assert bits & ssd.DEV_A_NOT_NEG
+    assert np.all(y[:, 1] == 0) and np.all(fs[:, 1] == 0)
+    yr, fr = scan_oracle(s, heads=[0, 2])
+    check_bf16("segmented good heads y", y[:, [0, 2]], yr)
+    check_bf16("segmented good heads final", fs[:, [0, 2]], fr)
+
+
+def test_segmented_needs_workspace():
+    s = I.make_scan_inputs([600], H=2, P=32, G=1, N=128, chunk_size=128, act="bf16", seed=145)
+    args = (dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C))
+    kw = dict(cu_seqlens=torch.from_numpy(s.cu_seqlens).cuda(), chunk_size=128, impl="tc",
+              D=dev(s.D), dt_bias=dev(s.dt_bias))
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ssd.SsdError) as e:   # forced split, workspace too small
+        ssd.chunk_scan(*args, seg_chunks=1, workspace=small, **kw)
+    assert e.value.code == 1
+    # with seg_chunks = 0 the same workspace just means "run unsplit"
+    y, _ = ssd.chunk_scan(*args, workspace=small, **kw)
+    yr, _ = scan_oracle(s)
+    check_bf16("unsplit fallback y", y.float().cpu().numpy(), yr)
+
+
 @pytest.mark.parametrize("impl", ["tc", "simt"])
 def test_A_not_negative_sets_status(impl):
     s = I.make_scan_inputs([140], H=3, P=32, G=1, N=128, chunk_size=128, act="bf16", seed=131,
@@ -154,22 +208,45 @@ def test_host_validation_errors():
 
 # ----------------------------------------------------------------------------- full sizes
 
-def test_mamba2_130m_layer_full():
-    """2 x 2048 tokens, H=24, P=64, G=1, N=128, chunk 256, initial states: whole output."""
+@pytest.mark.parametrize("seg", [0, -1])
+def test_mamba2_130m_layer_full(seg):
+    """2 x 2048 tokens, H=24, P=64, G=1, N=128, chunk 256, initial states: whole output,
+    as the library plans it (seg 0: split into segments) and as one chain per sequence."""
     s = I.scan_workload("mamba2_130m")
-    y, fs, bits = scan_gpu(s)
+    y, fs, bits = scan_gpu(s, seg_chunks=seg)
     assert bits == 0
     yr, fr = scan_oracle(s)
-    check_bf16("mamba2_130m y", y, yr)
-    check_bf16("mamba2_130m final", fs, fr)
+    check_bf16(f"mamba2_130m seg={seg} y", y, yr)
+    check_bf16(f"mamba2_130m seg={seg} final", fs, fr)
 
 
-def test_nemotron_h_varlen_sampled_heads():
+@pytest.mark.parametrize("seg", [0, 4])
+def test_nemotron_h_varlen_sampled_heads(seg):
     """4 packed sequences (8192, 3000, 517, 4675), H=128, G=8: heads from every group."""
     s = I.scan_workload("nemotron_h_varlen")
-    y, fs, bits = scan_gpu(s)
+    y, fs, bits = scan_gpu(s, seg_chunks=seg)
     assert bits == 0
     heads = [0, 17, 38, 63, 64, 90, 111, 127]
     yr, fr = scan_oracle(s, heads=heads)
     check_bf16("nemotron_h sampled y", y[:, heads], yr)
     check_bf16("nemotron_h sampled final", fs[:, heads], fr)
+
+
+def test_single_long_sequence_planned_split():
+    """One 16384-token sequence on 24 heads: the planner splits it into segments (48 CTAs
+    of 128 chunks would leave most SMs idle); sampled heads against the oracle, and the
+    whole output against the unsplit chain."""
+    s = I.scan_workload("mamba2_130m", seqlens=[16384])
+    x = dev(s.x)
+    assert ssd.chunk_scan_workspace_size(x, dev(s.B), dev(s.C),
+                                         cu_seqlens=torch.from_numpy(s.cu_seqlens).cuda(),
+                                         chunk_size=s.chunk_size) > 0
+    y, fs, bits = scan_gpu(s)
+    assert bits == 0
+    heads = [0, 11, 23]
+    yr, fr = scan_oracle(s, heads=heads)
+    check_bf16("single 16384 split y", y[:, heads], yr)
+    check_bf16("single 16384 split final", fs[:, heads], fr)
+    y1, f1, _ = scan_gpu(s, seg_chunks=-1)
+    check_bf16("single 16384 split vs unsplit y", y, y1)
+    check_bf16("single 16384 split vs unsplit final", fs, f1)
