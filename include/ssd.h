@@ -166,6 +166,29 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream
 SSD_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args);
 
 /* ------------------------------------------------------------------------------------
+ * ssd_chunk_scan_static_ws -- ssd_chunk_scan for callers that cannot allocate device
+ * memory at call time (a C host runtime with no device allocator of its own, or a caller
+ * that keeps allocator calls off its latency path).  The Mamba2 pages have no
+ * counterpart: it exists only so that such callers still get the split scan.
+ *
+ * Same arguments, results and errors as ssd_chunk_scan, except that the workspace is a
+ * 16 MiB device array owned by the library (part of its image, one per device):
+ *   - args->workspace must be NULL and workspace_bytes 0 (else SSD_ERR_INVALID_ARG);
+ *   - a call whose plan wants more than 16 MiB (ssd_chunk_scan_workspace_size) returns
+ *     SSD_ERR_UNSUPPORTED before launching anything: pass seg_chunks = -1 (no split) or
+ *     use ssd_chunk_scan with a workspace of the caller's;
+ *   - nothing in the array needs clearing between calls;
+ *   - the array is shared by every call on a device: calls that can overlap in time (on
+ *     different streams, or from different threads) race on it and must be ordered by
+ *     the caller;
+ *   - the first call on each device looks the array's address up (with that device
+ *     current), which may load this library's module onto the device: make that first
+ *     call before any stream capture is begun.
+ * Never allocates (no cudaMalloc, no allocating library routine); never synchronises.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * ssd_state_update -- one decode token per request on a pooled state cache,
  * vt::Mamba2StateUpdate of [vllm.cpp #566]; the pool is [atlas #69]'s SsmStatePool
  * layout, one fp32 [H, P, N] slot per concurrent request.

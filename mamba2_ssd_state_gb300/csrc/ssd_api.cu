@@ -66,6 +66,29 @@ ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream) {
   return launch_scan_simt(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_stream_t stream) {
+  ssd_status v = validate_scan(args);
+  if (v != SSD_OK) return v;
+  const ssd_scan_args& a = *args;
+  if (a.workspace || a.workspace_bytes) return SSD_ERR_INVALID_ARG;  // the library's own
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool tc_ok = scan_tc_supported(a);
+  if (a.impl == SSD_IMPL_TC || (a.impl == SSD_IMPL_AUTO && tc_ok)) {
+    if (!tc_ok) return SSD_ERR_UNSUPPORTED;
+    const size_t need = scan_tc_workspace_size(a);
+    if (need > scan_static_scratch_bytes()) return SSD_ERR_UNSUPPORTED;  // before any launch
+    ssd_scan_args b = a;
+    if (need > 0) {
+      b.workspace = scan_static_scratch();
+      if (!b.workspace) return SSD_ERR_CUDA;
+      b.workspace_bytes = scan_static_scratch_bytes();
+    }
+    return launch_scan_tc(b, st);
+  }
+  if (a.N > 256) return SSD_ERR_UNSUPPORTED;
+  return launch_scan_simt(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args) {
   if (validate_scan(args) != SSD_OK) return 0;
   const ssd_scan_args& a = *args;

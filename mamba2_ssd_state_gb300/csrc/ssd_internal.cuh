@@ -43,4 +43,9 @@ bool scan_tc_supported(const ssd_scan_args& a);
 size_t scan_tc_workspace_size(const ssd_scan_args& a);
 ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s);
 
+// Library-owned scan scratch (scan_noalloc.cu): its size, and its address on the current
+// device (NULL if the lookup failed).
+size_t scan_static_scratch_bytes();
+void* scan_static_scratch();
+
 }  // namespace ssd

@@ -69,6 +69,8 @@ def load_library(path: str | None = None):
         lib.ssd_chunk_scan.argtypes = [ctypes.POINTER(ScanArgs), _vp]
         lib.ssd_chunk_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs)]
         lib.ssd_chunk_scan_workspace_size.restype = ctypes.c_size_t
+        lib.ssd_chunk_scan_static_ws.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+        lib.ssd_chunk_scan_static_ws.restype = ctypes.c_int
         lib.ssd_state_update.argtypes = [ctypes.POINTER(UpdateArgs), _vp]
         lib.gated_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_float,
                                       ctypes.c_int, ctypes.c_int, _vp]

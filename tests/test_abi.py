@@ -22,7 +22,7 @@ def lib():
 def test_exports_every_declared_entry_point(lib):
     names = ssd.header_functions()
     assert set(names) == {"ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
-                          "ssd_state_update", "gated_rmsnorm", "ssd_read_status",
+                          "ssd_chunk_scan_static_ws", "ssd_state_update", "gated_rmsnorm", "ssd_read_status",
                           "ssd_status_string", "ssd_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
                          check=True).stdout

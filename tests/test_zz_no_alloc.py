@@ -1,0 +1,101 @@
+"""ssd_chunk_scan_static_ws: the scan entry point that allocates nothing (its split-scan
+workspace is a 16 MiB device array inside the library).
+
+Collected last on purpose: it must pass after the rest of the suite has run on the same
+device, as well as alone.  The GPU test calls the new entry through the C ABI twice in a
+row on two split workloads and holds each result to the bf16 bar against the existing
+entry point run with a caller-owned workspace.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from mamba2_ssd_state_gb300 import inputs as I
+from mamba2_ssd_state_gb300 import ssd
+from tolerance import check_bf16
+
+SCRATCH_BYTES = 16 << 20
+
+
+def _args(x, dt, A, B, C, cu, chunk_size, *, D=None, dt_bias=None, init=None, y=None,
+          fs=None, status=None, seg_chunks=0):
+    """ssd_scan_args for the given tensors (same marshalling as ssd.chunk_scan)."""
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    a = ssd.ScanArgs()
+    a.struct_size = ctypes.sizeof(ssd.ScanArgs)
+    a.x, a.x_stride_t = ssd._ptr(x), H * P
+    a.dt, a.dt_bias, a.dt_softplus = ssd._ptr(dt), ssd._ptr(dt_bias), 1
+    a.A, a.D = ssd._ptr(A), ssd._ptr(D)
+    a.B, a.B_stride_t = ssd._ptr(B), G * N
+    a.C, a.C_stride_t = ssd._ptr(C), G * N
+    a.initial_states = ssd._ptr(init)
+    a.cu_seqlens = ssd._ptr(cu)
+    a.nseq, a.T, a.H, a.P, a.G, a.N = cu.shape[0] - 1, T, H, P, G, N
+    a.chunk_size = chunk_size
+    a.act_dtype = ssd._act(x)
+    a.y, a.final_states, a.d_status = ssd._ptr(y), ssd._ptr(fs), ssd._ptr(status)
+    a.seg_chunks = seg_chunks
+    return a
+
+
+def test_static_ws_rejects_oversize_plans_and_caller_workspace():
+    """Host-side checks, before any launch: a plan wanting more than 16 MiB, and a
+    caller workspace passed to the entry that uses its own."""
+    lib = ssd.load_library()
+    a = ssd.ScanArgs()
+    a.struct_size = ctypes.sizeof(ssd.ScanArgs)
+    a.x = a.dt = a.A = a.B = a.C = a.cu_seqlens = a.y = 0x1000
+    a.act_dtype = ssd.SSD_BF16
+    a.nseq, a.T, a.H, a.P, a.G, a.N, a.chunk_size = 1, 65536, 128, 64, 8, 128, 256
+    a.seg_chunks = 8          # 64 segments of 4 MiB states
+    assert lib.ssd_chunk_scan_workspace_size(ctypes.byref(a)) > SCRATCH_BYTES
+    assert lib.ssd_chunk_scan_static_ws(ctypes.byref(a), None) == 2      # UNSUPPORTED
+    a.seg_chunks = -1
+    a.workspace, a.workspace_bytes = 0x1000, 256
+    assert lib.ssd_chunk_scan_static_ws(ctypes.byref(a), None) == 1      # INVALID_ARG
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", ["single_16384_planned", "varlen_seg2"])
+def test_static_ws_matches_caller_workspace_twice(case):
+    lib = ssd.load_library()
+    if case == "single_16384_planned":
+        s = I.scan_workload("mamba2_130m", seqlens=[16384])
+        seg = 0
+    else:
+        s = I.make_scan_inputs([700, 129, 1, 0, 300, 1000, 257, 128, 385], H=4, P=64, G=2,
+                               N=128, chunk_size=256, act="bf16", seed=151, init="all")
+        seg = 2
+    dev = torch.device("cuda")
+    T_ = lambda t: torch.from_numpy(np.ascontiguousarray(t.values)).to(
+        dev, torch.bfloat16 if t.dtype == "bf16" else torch.float32)
+    x, dt, A, B, C, D, bias, init = (T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D, s.dt_bias,
+                                                     s.initial_states))
+    cu = torch.from_numpy(s.cu_seqlens).to(dev)
+    need = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu, chunk_size=s.chunk_size,
+                                         seg_chunks=seg)
+    assert 0 < need <= SCRATCH_BYTES          # the case does use the scratch
+    y_ref, f_ref = ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=D,
+                                  dt_bias=bias, initial_states=init, seg_chunks=seg)
+    torch.cuda.synchronize()
+    y_ref, f_ref = y_ref.float().cpu().numpy(), f_ref.cpu().numpy()
+    for call in range(2):
+        y = torch.full_like(x, float("nan"))
+        fs = torch.full((s.nseq, s.H, s.P, s.N), float("nan"), device=dev)
+        status = ssd.new_status(dev)
+        a = _args(x, dt, A, B, C, cu, s.chunk_size, D=D, dt_bias=bias, init=init, y=y, fs=fs,
+                  status=status, seg_chunks=seg)
+        rc = lib.ssd_chunk_scan_static_ws(ctypes.byref(a),
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, ssd_status(lib, rc)
+        rc, bits = ssd.read_status(status)
+        assert bits == 0
+        check_bf16(f"{case} call {call} y", y.float().cpu().numpy(), y_ref)
+        check_bf16(f"{case} call {call} final", fs.cpu().numpy(), f_ref)
+
+
+def ssd_status(lib, rc):
+    return lib.ssd_status_string(rc).decode()
