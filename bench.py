@@ -376,7 +376,61 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
         "algorithmic_bytes_per_launch": ub, "achieved_gbs": ub / (us / 1e6) / 1e9,
         "peak_gbs": hbm_peak, "frac": ub / (us / 1e6) / 1e9 / hbm_peak,
         "peak_kind": f"{peak_kind} hbm copy"}
-    del pool, args
+    # fused decode layer step (update + D + gated norm, 8 norm groups of 1024) on the
+    # same pool and batch, against the two separate launches
+    z = torch.randn((batch, H * P), device=dev).to(torch.bfloat16)
+    wn = (1 + 0.1 * torch.randn(H * P, device=dev)).to(torch.bfloat16)
+    yb = torch.empty((batch, H, P), dtype=torch.bfloat16, device=dev)
+
+    def timed(fn, n=iters):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(n):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) * 1e3 / n
+
+    us_f = timed(lambda: ssd.decode_layer_step(*args, z, wn, group_size=1024, **kw))
+    us_s = timed(lambda: ssd.gated_rmsnorm(ssd.state_update(*args, y=yb, **kw).view(batch, H * P),
+                                           z, wn, group_size=1024))
+    lb = ub + batch * H * P * 2 * 2 + H * P * 2  # + z in, out written (y stays on chip)
+    res["decode_layer_step"] = {
+        "workload": "update + D + gated RMSNorm (8 groups of 1024) fused, batch 256 on the "
+                    "512-slot pool", "avg_launch_us": us_f, "unfused_us": us_s,
+        "algorithmic_bytes_per_launch": lb, "achieved_gbs": lb / (us_f / 1e6) / 1e9,
+        "frac": lb / (us_f / 1e6) / 1e9 / hbm_peak, "peak_kind": f"{peak_kind} hbm copy"}
+    # multi-token update: 4 draft tokens for 64 requests, keeping every per-token state
+    ntok, bm = 4, 64
+    mi = I.padded_permutation(S, bm, seed=3200)
+    mu = I.make_update_inputs(1, mi, H, P, G, N, act="bf16", seed=3210, ntok=ntok,
+                              pool_values=np.zeros((1, H, P, N), np.float32))
+    inter = torch.empty((bm, ntok, H, P, N), device=dev)
+    margs = (pool, torch.from_numpy(mi).to(dev), T_(mu.x), T_(mu.dt), T_(mu.A), T_(mu.B),
+             T_(mu.C))
+    us_m = timed(lambda: ssd.state_update_multi(*margs, D=T_(mu.D), dt_bias=T_(mu.dt_bias),
+                                                inter_states=inter))
+    act_m = int((mi >= 0).sum())
+    mb = act_m * H * P * N * 4 * (2 + ntok) + bm * ntok * (4 * H * P + 4 * G * N + 4 * H)
+    res["state_update_multi"] = {
+        "workload": "4 tokens per request, 64 requests (10% rows -1) on the 512-slot pool, "
+                    "state after every token kept", "avg_launch_us": us_m,
+        "algorithmic_bytes_per_launch": mb, "achieved_gbs": mb / (us_m / 1e6) / 1e9,
+        "frac": mb / (us_m / 1e6) / 1e9 / hbm_peak, "peak_kind": f"{peak_kind} hbm copy"}
+    # slot copy: 64 states of 4 MiB into a snapshot pool
+    snap = torch.empty((64, H, P, N), device=dev)
+    ci = torch.from_numpy(I.padded_permutation(S, 64, seed=3300)).to(dev).abs()
+    co = torch.arange(64, dtype=torch.int32, device=dev)
+    us_c = timed(lambda: ssd.state_copy(pool, ci, snap, co))
+    cb = 64 * H * P * N * 4 * 2
+    res["state_copy"] = {
+        "workload": "64 slots of [128,64,128] fp32 copied pool -> snapshot pool",
+        "avg_launch_us": us_c, "algorithmic_bytes_per_launch": cb,
+        "achieved_gbs": cb / (us_c / 1e6) / 1e9, "frac": cb / (us_c / 1e6) / 1e9 / hbm_peak,
+        "peak_kind": f"{peak_kind} hbm copy"}
+    del pool, args, inter, snap
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def time_scan(s, **kw):

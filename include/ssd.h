@@ -11,7 +11,8 @@
  *       "Carried forward" and the #675 message).
  *   [atlas #69] the pull-request page "feat(spark-server): inject tool-call parser
  *       system prompt" (atlas PR #69), whose SsmStatePool keeps one fp32 SSM state
- *       slot per concurrent decode request.
+ *       slot per concurrent decode request, beside an SsmSnapshotPool of prefix-cache
+ *       state snapshots and a decode-rollback ring (its notes on the two SSM pools).
  *   [Mamba-2] Dao & Gu, "Transformers are SSMs" (2024), the SSD layer, for the
  *       recurrence itself, which the pages name but do not print.
  *
@@ -230,6 +231,67 @@ typedef struct {
 } ssd_update_args;
 
 SSD_API ssd_status ssd_state_update(const ssd_update_args* args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_state_update_multi -- ntok decode tokens per request in one pass over the state:
+ * the selective state update of ssd_state_update applied ntok times in order (a
+ * speculative step's draft tokens, or a short chunk), the state kept in registers
+ * between tokens.  With inter_states the state after every token is also written, so
+ * a caller that accepts only m of the ntok tokens can restore the m-th one into the
+ * pool with ssd_state_copy -- the decode-rollback ring of [atlas #69].
+ *
+ * Arguments: as ssd_state_update, with one more leading token axis on the per-token
+ * tensors: x [batch, ntok, H, P], dt [batch, ntok, H], B, C [batch, ntok, G, N],
+ * y [batch, ntok, H, P] (token t of request b at row b * ntok + t).  inter_states: fp32
+ * [batch, ntok, H, P, N], dense, 16-byte aligned, or NULL.  The pool slot receives the
+ * state after the last token.  Rows with index -1, out-of-range slots and heads with A
+ * not < 0 leave the pool and inter_states untouched and give y = 0 for every token
+ * (status bits as ssd_state_update).  ntok >= 1; N in {16, 32, 64, 128}
+ * (else SSD_ERR_UNSUPPORTED).  Duplicate slots in one call race, as in ssd_state_update.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status ssd_state_update_multi(const ssd_update_args* args, int32_t ntok,
+                                          float* inter_states, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_decode_layer_step -- one decode token of a Mamba2 mixer after its projections:
+ * the state update with D skip of ssd_state_update, then the silu-gated RMSNorm of
+ * gated_rmsnorm on the result (vt::Mamba2StateUpdate followed by vt::RmsNormGatedGroup,
+ * [vllm.cpp #566]), fused: y stays on chip.  A thread-block cluster of up to 8 CTAs owns
+ * one norm group of one request; the CTAs exchange their partial sums of g^2 through
+ * distributed shared memory.
+ *
+ * Arguments: args as ssd_state_update, except that args->y may be NULL (then y is not
+ * written); z [batch, H*P] act_dtype; norm_weight [H*P] weight_dtype; out [batch, H*P]
+ * act_dtype.  group_size: channels per norm group, a multiple of P dividing H*P (a norm
+ * group is a whole number of heads).  eps >= 0.  Rows with index -1 (and heads that
+ * are skipped) contribute y = 0, so their out is 0.  N in {16, 32, 64, 128}.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status ssd_decode_layer_step(const ssd_update_args* args, const void* z,
+                                         const void* norm_weight, ssd_dtype weight_dtype,
+                                         int32_t group_size, float eps, void* out,
+                                         ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_state_copy -- copy whole state slots between two pools: for every i < n with
+ * src_idx[i] >= 0 and dst_idx[i] >= 0, dst slot dst_idx[i] becomes a copy of src slot
+ * src_idx[i] (slot_elems fp32 values).  This is the state copy between [atlas #69]'s
+ * working pool (SsmStatePool) and its prefix-cache snapshots (SsmSnapshotPool), and the
+ * rollback of ssd_state_update_multi (its batch * ntok intermediate states form a valid
+ * source pool).
+ *
+ * Arguments: pools fp32, device, with slot strides in elements (0 = slot_elems),
+ * 16-byte aligned, slot_elems and strides multiples of 4 (else SSD_ERR_UNSUPPORTED);
+ * src_slots / dst_slots: slot counts for the bounds check; src_idx, dst_idx: int32 [n],
+ * device.  A -1 on either side skips the pair; an index outside [-1, slots) sets
+ * SSD_DEV_INDEX_OOR and skips the pair.  The two pools may be one pool.  Destination
+ * slots must be distinct and no destination may be a source of the same call (the
+ * copies run concurrently).  n <= 65535.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status ssd_state_copy(const float* src_pool, int64_t src_slot_stride,
+                                  int32_t src_slots, const int32_t* src_idx, float* dst_pool,
+                                  int64_t dst_slot_stride, int32_t dst_slots,
+                                  const int32_t* dst_idx, int32_t n, int64_t slot_elems,
+                                  uint32_t* d_status, ssd_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * gated_rmsnorm -- silu-gated RMSNorm with per-group variance, vt::RmsNormGatedGroup of

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libssd.so")
 ROOT = os.path.dirname(HERE)
 SOURCES = ["ssd_api.cu", "state_update.cu", "gated_rmsnorm.cu", "scan_simt.cu", "scan_tc.cu",
-           "scan_noalloc.cu"]
+           "scan_noalloc.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

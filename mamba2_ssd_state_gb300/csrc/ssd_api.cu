@@ -103,6 +103,67 @@ ssd_status ssd_state_update(const ssd_update_args* args, ssd_stream_t stream) {
   return launch_state_update(*args, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status ssd_state_copy(const float* src_pool, int64_t src_slot_stride, int32_t src_slots,
+                          const int32_t* src_idx, float* dst_pool, int64_t dst_slot_stride,
+                          int32_t dst_slots, const int32_t* dst_idx, int32_t n,
+                          int64_t slot_elems, uint32_t* d_status, ssd_stream_t stream) {
+  if (n < 0 || slot_elems < 1 || src_slots < 1 || dst_slots < 1) return SSD_ERR_INVALID_ARG;
+  if (n == 0) return SSD_OK;
+  if (!src_pool || !dst_pool || !src_idx || !dst_idx) return SSD_ERR_INVALID_ARG;
+  const int64_t ss = src_slot_stride ? src_slot_stride : slot_elems;
+  const int64_t ds = dst_slot_stride ? dst_slot_stride : slot_elems;
+  if (ss < slot_elems || ds < slot_elems) return SSD_ERR_INVALID_ARG;
+  // float4 copies: 16-byte aligned slots
+  if (slot_elems % 4 || ss % 4 || ds % 4 || ((uintptr_t)src_pool & 15u) ||
+      ((uintptr_t)dst_pool & 15u))
+    return SSD_ERR_UNSUPPORTED;
+  if (n > 65535) return SSD_ERR_UNSUPPORTED;  // grid limit
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_state_copy(src_pool, ss, src_slots, src_idx, dst_pool, ds, dst_slots, dst_idx, n,
+                           slot_elems, d_status, st) == cudaSuccess
+             ? SSD_OK
+             : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_state_update_multi(const ssd_update_args* args, int32_t ntok,
+                                  float* inter_states, ssd_stream_t stream) {
+  ssd_status v = validate_update(args);
+  if (v != SSD_OK) return v;
+  if (ntok < 1) return SSD_ERR_INVALID_ARG;
+  const ssd_update_args& a = *args;
+  if (a.batch == 0) return SSD_OK;
+  if (!decode_n_supported(a.N)) return SSD_ERR_UNSUPPORTED;
+  if (a.slot_stride % 4 || ((uintptr_t)a.state_pool & 15u) || ((uintptr_t)inter_states & 15u))
+    return SSD_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_state_update_multi(a, ntok, inter_states, st) == cudaSuccess ? SSD_OK
+                                                                             : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_decode_layer_step(const ssd_update_args* args, const void* z,
+                                 const void* norm_weight, ssd_dtype weight_dtype,
+                                 int32_t group_size, float eps, void* out,
+                                 ssd_stream_t stream) {
+  if (!args || args->struct_size < sizeof(ssd_update_args)) return SSD_ERR_INVALID_ARG;
+  ssd_update_args chk = *args;  // y is optional here
+  if (!chk.y) chk.y = out;
+  ssd_status v = validate_update(&chk);
+  if (v != SSD_OK) return v;
+  const ssd_update_args& a = *args;
+  if (!norm_weight || bad_dtype(weight_dtype) || !(eps >= 0.f)) return SSD_ERR_INVALID_ARG;
+  if (group_size < a.P || group_size % a.P || (a.H * a.P) % group_size)
+    return SSD_ERR_INVALID_ARG;
+  if (a.batch > 0 && (!z || !out)) return SSD_ERR_INVALID_ARG;
+  if (a.batch == 0) return SSD_OK;
+  if (!decode_n_supported(a.N)) return SSD_ERR_UNSUPPORTED;
+  if (a.slot_stride % 4 || ((uintptr_t)a.state_pool & 15u)) return SSD_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_decode_layer(a, z, norm_weight, weight_dtype, group_size, eps, out, st) ==
+                 cudaSuccess
+             ? SSD_OK
+             : SSD_ERR_CUDA;
+}
+
 ssd_status gated_rmsnorm(const void* x, const void* z, const void* weight, void* out,
                          int64_t rows, int32_t d, int32_t group_size, float eps, ssd_dtype act,
                          ssd_dtype wt, ssd_stream_t stream) {

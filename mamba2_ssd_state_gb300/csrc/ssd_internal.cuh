@@ -43,6 +43,19 @@ bool scan_tc_supported(const ssd_scan_args& a);
 size_t scan_tc_workspace_size(const ssd_scan_args& a);
 ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s);
 
+// Decode-side ops (decode.cu).
+bool decode_n_supported(int N);
+int decode_layer_cluster(int heads_per_group);
+cudaError_t launch_state_copy(const float* src, int64_t src_stride, int src_slots,
+                              const int32_t* src_idx, float* dst, int64_t dst_stride,
+                              int dst_slots, const int32_t* dst_idx, int n, int64_t slot_elems,
+                              uint32_t* status, cudaStream_t st);
+cudaError_t launch_state_update_multi(const ssd_update_args& a, int ntok, float* inter,
+                                      cudaStream_t st);
+cudaError_t launch_decode_layer(const ssd_update_args& a, const void* z, const void* w,
+                                ssd_dtype wt, int group_size, float eps, void* out,
+                                cudaStream_t st);
+
 // Library-owned scan scratch (scan_noalloc.cu): its size, and its address on the current
 // device (NULL if the lookup failed).
 size_t scan_static_scratch_bytes();

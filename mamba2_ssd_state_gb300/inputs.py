@@ -173,22 +173,25 @@ def padded_permutation(num_slots, batch, pad_frac=0.1, seed=3000):
 
 
 def make_update_inputs(num_slots, state_indices, H, P, G, N, act="bf16", seed=3000,
-                       pool_values=None) -> UpdateInputs:
+                       pool_values=None, ntok=None) -> UpdateInputs:
+    """Decode inputs for one token per request, or (ntok given) ntok tokens per request
+    with a token axis after the request axis: x [batch, ntok, H, P] and so on."""
     idx = np.asarray(state_indices, dtype=np.int32)
     batch = idx.shape[0]
+    bt = (batch,) if ntok is None else (batch, ntok)
     rng = lambda k: np.random.default_rng(seed * 100 + k)  # noqa: E731
     u = UpdateInputs(num_slots, H, P, G, N, act)
     if pool_values is None:
         pool_values = rng(9).standard_normal((num_slots, H, P, N), dtype=np.float32)
     u.pool = _t(pool_values, "f32")
     u.state_indices = idx
-    u.x = _t(rng(1).standard_normal((batch, H, P), dtype=np.float32), act)
-    u.dt = _t(rng(2).standard_normal((batch, H), dtype=np.float32), "f32")
+    u.x = _t(rng(1).standard_normal((*bt, H, P), dtype=np.float32), act)
+    u.dt = _t(rng(2).standard_normal((*bt, H), dtype=np.float32), "f32")
     u.dt_bias = _t(np.log(np.expm1(rng(3).uniform(1e-3, 0.1, size=H))), "f32")
     u.A = _t(-np.exp(rng(4).uniform(0.0, np.log(16.0), size=H)), "f32")
     inv = 1.0 / np.sqrt(N)
-    u.B = _t(rng(5).standard_normal((batch, G, N), dtype=np.float32) * inv, act)
-    u.C = _t(rng(6).standard_normal((batch, G, N), dtype=np.float32) * inv, act)
+    u.B = _t(rng(5).standard_normal((*bt, G, N), dtype=np.float32) * inv, act)
+    u.C = _t(rng(6).standard_normal((*bt, G, N), dtype=np.float32) * inv, act)
     u.D = _t(rng(7).standard_normal(H, dtype=np.float32), "f32")
     return u
 

@@ -71,6 +71,14 @@ def load_library(path: str | None = None):
         lib.ssd_chunk_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssd_chunk_scan_static_ws.argtypes = [ctypes.POINTER(ScanArgs), _vp]
         lib.ssd_chunk_scan_static_ws.restype = ctypes.c_int
+        lib.ssd_state_update_multi.argtypes = [ctypes.POINTER(UpdateArgs), _i32, _vp, _vp]
+        lib.ssd_state_update_multi.restype = ctypes.c_int
+        lib.ssd_decode_layer_step.argtypes = [ctypes.POINTER(UpdateArgs), _vp, _vp, ctypes.c_int,
+                                              _i32, ctypes.c_float, _vp, _vp]
+        lib.ssd_decode_layer_step.restype = ctypes.c_int
+        lib.ssd_state_copy.argtypes = [_vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _i64,
+                                       _vp, _vp]
+        lib.ssd_state_copy.restype = ctypes.c_int
         lib.ssd_state_update.argtypes = [ctypes.POINTER(UpdateArgs), _vp]
         lib.gated_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _i32, ctypes.c_float,
                                       ctypes.c_int, ctypes.c_int, _vp]
@@ -225,6 +233,117 @@ def chunk_scan_workspace_size(x, B, C, *, cu_seqlens, chunk_size, impl="auto", p
     a.chunk_size, a.act_dtype = int(chunk_size), _act(x)
     a.impl, a.p_block, a.seg_chunks = IMPL[impl], int(p_block), int(seg_chunks)
     return int(lib.ssd_chunk_scan_workspace_size(ctypes.byref(a)))
+
+
+def _update_args(state_pool, state_indices, x, dt, A, B, C, D, dt_bias, dt_softplus, y,
+                 status, tok_shape):
+    """ssd_update_args for one decode call; tok_shape is () or (ntok,): the token axes
+    between the request axis and the per-token dimensions of x, dt, B, C and y."""
+    num_slots, H, P, N = state_pool.shape
+    batch = state_indices.shape[0]
+    G = B.shape[-2]
+    dev = x.device
+    bt = (batch, *tok_shape)
+    _check(state_pool, "state_pool", torch.float32, None, dev)
+    _check(state_indices, "state_indices", torch.int32, (batch,), dev)
+    _check(x, "x", None, (*bt, H, P), dev)
+    _check(dt, "dt", torch.float32, (*bt, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(D, "D", torch.float32, (H,), dev)
+    _check(dt_bias, "dt_bias", torch.float32, (H,), dev)
+    _check(B, "B", x.dtype, (*bt, G, N), dev)
+    _check(C, "C", x.dtype, (*bt, G, N), dev)
+    _check(y, "y", x.dtype, (*bt, H, P), dev)
+    for t, nm in ((x, "x"), (dt, "dt"), (B, "B"), (C, "C"), (state_indices, "state_indices"),
+                  (y, "y")):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    if any(state_pool.stride(d) != s for d, s in ((3, 1), (2, N), (1, P * N))):
+        raise ValueError("state_pool slots must be dense [H,P,N]")
+    a = UpdateArgs()
+    a.struct_size = ctypes.sizeof(UpdateArgs)
+    a.state_pool, a.slot_stride, a.num_slots = _ptr(state_pool), int(state_pool.stride(0)), num_slots
+    a.state_indices, a.batch = _ptr(state_indices), batch
+    a.x, a.dt, a.dt_bias, a.dt_softplus = _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus))
+    a.A, a.B, a.C, a.D, a.y = _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y)
+    a.H, a.P, a.G, a.N = H, P, G, N
+    a.act_dtype = _act(x)
+    a.d_status = _ptr(status)
+    return a
+
+
+def state_update_multi(state_pool, state_indices, x, dt, A, B, C, *, D=None, dt_bias=None,
+                       dt_softplus=True, y=None, inter_states=None, status=None, stream=None):
+    """ntok decode tokens per request in one pass (ssd_state_update_multi in ssd.h).
+
+    x [batch,ntok,H,P]; dt [batch,ntok,H]; B/C [batch,ntok,G,N].  inter_states: None, True
+    (allocate) or an fp32 [batch,ntok,H,P,N] tensor receiving the state after each token.
+    Returns (y [batch,ntok,H,P], inter_states)."""
+    lib = load_library()
+    batch, ntok, H, P = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    if inter_states is True:
+        inter_states = torch.empty((batch, ntok, H, P, state_pool.shape[3]), dtype=torch.float32,
+                                   device=x.device)
+    if inter_states is not None:
+        _check(inter_states, "inter_states", torch.float32,
+               (batch, ntok, H, P, state_pool.shape[3]), x.device)
+        if not inter_states.is_contiguous():
+            raise ValueError("inter_states must be contiguous")
+    a = _update_args(state_pool, state_indices, x, dt, A, B, C, D, dt_bias, dt_softplus, y, status,
+                     (ntok,))
+    _raise(lib.ssd_state_update_multi(ctypes.byref(a), ntok, _ptr(inter_states), _stream(stream)),
+           "ssd_state_update_multi")
+    return y, inter_states
+
+
+def decode_layer_step(state_pool, state_indices, x, dt, A, B, C, z, norm_weight, *, group_size,
+                      eps=1e-5, D=None, dt_bias=None, dt_softplus=True, y=None, out=None,
+                      status=None, stream=None):
+    """State update + D skip + gated RMSNorm of one decode token, fused
+    (ssd_decode_layer_step in ssd.h).  z [batch,H*P]; norm_weight [H*P].  y (optional)
+    receives the pre-norm output.  Returns out [batch,H*P]."""
+    lib = load_library()
+    batch, H, P = x.shape
+    dev = x.device
+    _check(z, "z", x.dtype, (batch, H * P), dev)
+    _check(norm_weight, "norm_weight", None, (H * P,), dev)
+    for t, nm in ((z, "z"), (norm_weight, "norm_weight")):
+        if not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    if out is None:
+        out = torch.empty((batch, H * P), dtype=x.dtype, device=dev)
+    _check(out, "out", x.dtype, (batch, H * P), dev)
+    a = _update_args(state_pool, state_indices, x, dt, A, B, C, D, dt_bias, dt_softplus, y, status,
+                     ())
+    _raise(lib.ssd_decode_layer_step(ctypes.byref(a), _ptr(z), _ptr(norm_weight),
+                                     _act(norm_weight), int(group_size), float(eps), _ptr(out),
+                                     _stream(stream)), "ssd_decode_layer_step")
+    return out
+
+
+def state_copy(src_pool, src_idx, dst_pool, dst_idx, *, status=None, stream=None):
+    """dst_pool[dst_idx[i]] = src_pool[src_idx[i]] for every pair without a -1
+    (ssd_state_copy in ssd.h).  Pools fp32 [slots, ...] with dense slots."""
+    lib = load_library()
+    n = src_idx.shape[0]
+    dev = src_pool.device
+    _check(src_pool, "src_pool", torch.float32, None, dev)
+    _check(dst_pool, "dst_pool", torch.float32, None, dev)
+    _check(src_idx, "src_idx", torch.int32, (n,), dev)
+    _check(dst_idx, "dst_idx", torch.int32, (n,), dev)
+    slot = src_pool[0].numel()
+    if dst_pool[0].numel() != slot:
+        raise ValueError("source and destination slots differ in size")
+    for t, nm in ((src_pool, "src_pool"), (dst_pool, "dst_pool")):
+        if not t[0].is_contiguous():
+            raise ValueError(f"{nm} slots must be dense")
+    _raise(lib.ssd_state_copy(_ptr(src_pool), int(src_pool.stride(0)), src_pool.shape[0],
+                              _ptr(src_idx), _ptr(dst_pool), int(dst_pool.stride(0)),
+                              dst_pool.shape[0], _ptr(dst_idx), n, slot, _ptr(status),
+                              _stream(stream)), "ssd_state_copy")
+    return dst_pool
 
 
 def state_update(state_pool, state_indices, x, dt, A, B, C, *, D=None, dt_bias=None,

@@ -138,3 +138,59 @@ def gated_rmsnorm(x, z, weight, *, group_size, eps=1e-5):
     if rc != 0:
         raise ValueError(f"oracle_gated_rmsnorm rejected its arguments (rc={rc})")
     return out
+
+
+# ----------------------------------------------------------------- compositions
+# The decode-side ops below are defined by the single-token update and the gated norm
+# above (each pinned in tests/test_oracle_pins.py); here they are those definitions
+# applied in order, with nothing fused or reordered.
+
+def state_update_multi(pool, state_indices, x, dt, A, B, C, *, D=None, dt_bias=None,
+                       dt_softplus=True):
+    """ntok decode tokens per request: the single-token update applied token by token.
+    x [batch, ntok, H, P] etc.  Returns (new_pool, y [batch, ntok, H, P], inter
+    [batch, ntok, H, P, N] (state after each token, NaN where the row is skipped),
+    status_bits)."""
+    x, dt, B, C = (np.asarray(v) for v in (x, dt, B, C))
+    batch, ntok = x.shape[:2]
+    pool = np.array(pool, dtype=np.float64, order="C", copy=True)
+    num_slots, H, P, N = pool.shape
+    idx = np.asarray(state_indices, dtype=np.int32)
+    y = np.empty((batch, ntok, H, P))
+    inter = np.full((batch, ntok, H, P, N), np.nan)
+    st = 0
+    for t in range(ntok):
+        pool, y[:, t], s_t = state_update(pool, idx, x[:, t], dt[:, t], A, B[:, t], C[:, t], D=D,
+                                          dt_bias=dt_bias, dt_softplus=dt_softplus)
+        st |= s_t
+        for b in range(batch):
+            if 0 <= idx[b] < num_slots:
+                inter[b, t] = pool[idx[b]]
+    return pool, y, inter, st
+
+
+def decode_layer_step(pool, state_indices, x, dt, A, B, C, z, norm_weight, *, group_size,
+                      eps=1e-5, D=None, dt_bias=None, dt_softplus=True):
+    """The single-token update, then the gated norm of its output.  Returns
+    (new_pool, y [batch, H, P], out [batch, H*P], status_bits)."""
+    pool, y, st = state_update(pool, state_indices, x, dt, A, B, C, D=D, dt_bias=dt_bias,
+                               dt_softplus=dt_softplus)
+    batch, H, P = y.shape
+    out = gated_rmsnorm(y.reshape(batch, H * P), z, norm_weight, group_size=group_size, eps=eps)
+    return pool, y, out, st
+
+
+def state_copy(src_pool, src_idx, dst_pool, dst_idx):
+    """Slot copy: for each pair with both indices >= 0, the destination slot becomes the
+    source slot; a pair with an index outside [-1, slots) is skipped and raises the
+    out-of-range bit (2).  Returns (new_dst, status_bits)."""
+    src = np.asarray(src_pool)
+    dst = np.array(dst_pool, copy=True)
+    st = 0
+    for s, d in zip(np.asarray(src_idx).tolist(), np.asarray(dst_idx).tolist()):
+        if s < -1 or s >= src.shape[0] or d < -1 or d >= dst.shape[0]:
+            st |= 2
+            continue
+        if s >= 0 and d >= 0:
+            dst[d] = src[s]
+    return dst, st

@@ -22,7 +22,8 @@ def lib():
 def test_exports_every_declared_entry_point(lib):
     names = ssd.header_functions()
     assert set(names) == {"ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
-                          "ssd_chunk_scan_static_ws", "ssd_state_update", "gated_rmsnorm", "ssd_read_status",
+                          "ssd_chunk_scan_static_ws", "ssd_state_update",
+                          "ssd_state_update_multi", "ssd_decode_layer_step", "ssd_state_copy", "gated_rmsnorm", "ssd_read_status",
                           "ssd_status_string", "ssd_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
                          check=True).stdout
@@ -120,6 +121,30 @@ def test_norm_rejects_bad_arguments(lib):
     assert lib.gated_rmsnorm(p, p, p, p, 4, 64, 64, -1.0, 1, 1, None) == 1
     assert lib.gated_rmsnorm(p, p, p, p, 4, 64, 64, 1e-5, 3, 1, None) == 1
     assert lib.ssd_read_status(None, 1, None, None) == 1
+
+
+def test_decode_ops_reject_bad_arguments(lib):
+    """Host-side validation of the decode-side entry points (nothing is launched)."""
+    a = ssd.UpdateArgs()
+    a.struct_size = ctypes.sizeof(ssd.UpdateArgs)
+    a.state_pool = a.A = a.state_indices = a.x = a.dt = a.B = a.C = a.y = 0x1000
+    a.num_slots, a.batch, a.H, a.P, a.G, a.N = 4, 2, 4, 16, 2, 16
+    p = 0x1000
+    assert lib.ssd_state_update_multi(ctypes.byref(a), 0, None, None) == 1        # ntok 0
+    a.N = 48
+    assert lib.ssd_state_update_multi(ctypes.byref(a), 2, None, None) == 2        # N 48
+    a.N = 16
+    for gs in (24, 8, 48):   # not a multiple of P, below P, not dividing H*P
+        assert lib.ssd_decode_layer_step(ctypes.byref(a), p, p, 0, gs, 1e-5, p, None) == 1
+    assert lib.ssd_decode_layer_step(ctypes.byref(a), p, None, 0, 32, 1e-5, p, None) == 1
+    assert lib.ssd_decode_layer_step(ctypes.byref(a), p, p, 0, 32, -1.0, p, None) == 1
+    # slot copy: sizes, alignment, grid limit
+    assert lib.ssd_state_copy(p, 0, 2, p, p, 0, 2, p, -1, 64, None, None) == 1
+    assert lib.ssd_state_copy(p, 0, 2, p, p, 0, 2, p, 0, 64, None, None) == 0     # nothing
+    assert lib.ssd_state_copy(p, 32, 2, p, p, 0, 2, p, 1, 64, None, None) == 1    # stride
+    assert lib.ssd_state_copy(p, 0, 2, p, p, 0, 2, p, 1, 6, None, None) == 2      # 6 % 4
+    assert lib.ssd_state_copy(p + 4, 0, 2, p, p, 0, 2, p, 1, 64, None, None) == 2  # align
+    assert lib.ssd_state_copy(p, 0, 2, p, p, 0, 2, p, 70000, 64, None, None) == 2
 
 
 def test_status_strings_and_version(lib):

@@ -334,3 +334,95 @@ def test_norm_without_gate(oracle_mod):
     ref = torch.nn.functional.rms_norm(torch.tensor(n.x.values, dtype=torch.float64), (d,),
                                        torch.tensor(n.weight.values, dtype=torch.float64), 1e-6)
     assert _rel(out, ref.numpy()) < 1e-13
+
+
+# ------------------------------------------------------------- decode-side compositions
+
+def test_multi_token_decode_equals_scan_from_the_slot(oracle_mod):
+    """k decode tokens on a slot are the k-token scan started from that slot's state: the
+    per-token update (applied k times) and the sequence scan are separate code paths of
+    the oracle.  Every intermediate state is the final state of the scan's prefix."""
+    H, P, G, N, S, k = 4, 3, 2, 5, 5, 6
+    idx = np.array([4, -1, 1], dtype=np.int32)
+    u = I.make_update_inputs(S, idx, H, P, G, N, act="f32", seed=61, ntok=k)
+    pool0 = u.pool.values.astype(np.float64)
+    newpool, y, inter, st = oracle_mod.state_update_multi(
+        pool0, idx, u.x.values, u.dt.values, u.A.values, u.B.values, u.C.values, D=u.D.values,
+        dt_bias=u.dt_bias.values)
+    assert st == 0
+    assert np.all(y[1] == 0.0) and np.all(np.isnan(inter[1]))
+    for b, slot in ((0, 4), (2, 1)):
+        ys, fs = oracle_mod.scan_seq(u.x.values[b], u.dt.values[b], u.A.values, u.B.values[b],
+                                     u.C.values[b], D=u.D.values, dt_bias=u.dt_bias.values,
+                                     initial_states=pool0[slot][None])
+        assert _rel(y[b], ys) < 1e-12
+        assert _rel(newpool[slot], fs[0]) < 1e-12
+        for t in range(k):
+            _, ft = oracle_mod.scan_seq(u.x.values[b, :t + 1], u.dt.values[b, :t + 1],
+                                        u.A.values, u.B.values[b, :t + 1], u.C.values[b, :t + 1],
+                                        D=u.D.values, dt_bias=u.dt_bias.values,
+                                        initial_states=pool0[slot][None])
+            assert _rel(inter[b, t], ft[0]) < 1e-12
+    for slot in (0, 2, 3):
+        np.testing.assert_array_equal(newpool[slot], pool0[slot])
+
+
+def test_state_copy_invariants(oracle_mod):
+    """Copy and copy back restores the pool; -1 on either side skips; an out-of-range
+    index raises bit 2 and skips only its pair; slots not named stay identical."""
+    rng = np.random.default_rng(67)
+    src = rng.standard_normal((5, 2, 3, 4))
+    dst = rng.standard_normal((4, 2, 3, 4))
+    new, st = oracle_mod.state_copy(src, [3, -1, 0, 1], dst, [0, 2, -1, 3])
+    assert st == 0
+    np.testing.assert_array_equal(new[0], src[3])
+    np.testing.assert_array_equal(new[3], src[1])
+    for d in (1, 2):
+        np.testing.assert_array_equal(new[d], dst[d])
+    back, st = oracle_mod.state_copy(dst, [0, 3], new, [0, 3])
+    np.testing.assert_array_equal(back, dst)
+    new2, st = oracle_mod.state_copy(src, [5, 2], dst, [1, 1])
+    assert st == 2
+    np.testing.assert_array_equal(new2[1], src[2])
+    new3, st = oracle_mod.state_copy(src, [0], dst, [-2])
+    assert st == 2
+    np.testing.assert_array_equal(new3, dst)
+
+
+def test_decode_layer_output_has_unit_group_rms(oracle_mod):
+    """The fused decode step's output divided by the norm weight has, per row and norm
+    group, mean square mean(g^2) / (mean(g^2) + eps): 1 up to eps.  -1 rows give 0."""
+    H, P, G, N, S, gs = 4, 8, 2, 6, 5, 16
+    idx = np.array([2, -1, 0], dtype=np.int32)
+    u = I.make_update_inputs(S, idx, H, P, G, N, act="f32", seed=71)
+    n = I.make_norm_inputs(3, H * P, gs, act="f32", seed=73)
+    eps = 1e-5
+    pool, y, out, st = oracle_mod.decode_layer_step(
+        u.pool.values, idx, u.x.values, u.dt.values, u.A.values, u.B.values, u.C.values,
+        n.z.values, n.weight.values, group_size=gs, eps=eps, D=u.D.values,
+        dt_bias=u.dt_bias.values)
+    assert st == 0
+    g = (y.reshape(3, H * P) * n.z.values / (1 + np.exp(-n.z.values.astype(np.float64))))
+    r = out / n.weight.values.astype(np.float64)
+    for b in (0, 2):
+        for k in range(H * P // gs):
+            sl = slice(k * gs, (k + 1) * gs)
+            ms = np.mean(g[b, sl] ** 2)
+            assert abs(np.mean(r[b, sl] ** 2) - ms / (ms + eps)) < 1e-12
+    assert np.all(out[1] == 0.0)
+
+
+def test_bf16_half_ulp_matches_rounding():
+    """The bf16 half-ulp the tests allow on bf16-stored outputs is the largest error of
+    rounding to bf16 (checked against torch's round-to-nearest-even conversion)."""
+    torch = pytest.importorskip("torch")
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from tolerance import bf16_half_ulp
+    v = (np.random.default_rng(79).standard_normal(20000) * np.exp2(
+        np.random.default_rng(80).integers(-10, 10, 20000))).astype(np.float32)
+    r = torch.tensor(v).to(torch.bfloat16).double().numpy()     # fp32 -> bf16, RNE
+    v = v.astype(np.float64)
+    assert np.all(np.abs(r - v) <= bf16_half_ulp(v))
+    assert np.max(np.abs(r - v) / bf16_half_ulp(v)) > 0.99   # and it is tight
+    assert bf16_half_ulp(16.3) == 2.0 ** -4
