@@ -155,8 +155,6 @@ ssd_status ssd_decode_layer_step(const ssd_update_args* args, const void* z,
     return SSD_ERR_INVALID_ARG;
   if (a.batch > 0 && (!z || !out)) return SSD_ERR_INVALID_ARG;
   if (a.batch == 0) return SSD_OK;
-  if (!decode_n_supported(a.N)) return SSD_ERR_UNSUPPORTED;
-  if (a.slot_stride % 4 || ((uintptr_t)a.state_pool & 15u)) return SSD_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return launch_decode_layer(a, z, norm_weight, weight_dtype, group_size, eps, out, st) ==
                  cudaSuccess

@@ -45,7 +45,6 @@ ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s);
 
 // Decode-side ops (decode.cu).
 bool decode_n_supported(int N);
-int decode_layer_cluster(int heads_per_group);
 cudaError_t launch_state_copy(const float* src, int64_t src_stride, int src_slots,
                               const int32_t* src_idx, float* dst, int64_t dst_stride,
                               int dst_slots, const int32_t* dst_idx, int n, int64_t slot_elems,

@@ -157,7 +157,7 @@ def _layer(u, n, gs, pool, wt=None, want_y=True):
 @pytest.mark.parametrize("H,P,G,gs,batch", [(128, 64, 8, 1024, 32), (24, 64, 1, 1536, 8),
                                             (6, 64, 2, 192, 5), (4, 32, 2, 32, 3)])
 def test_decode_layer_step_bf16(H, P, G, gs, batch):
-    """Norm groups of 16, 24, 3 and 1 heads: clusters of 8, 8, 1 and 1 CTAs."""
+    """Norm groups of 16, 24, 3 and 1 heads."""
     N, S = 128, batch + 7
     idx = I.padded_permutation(S, batch, seed=441 + batch)
     u = I.make_update_inputs(S, idx, H, P, G, N, act="bf16", seed=443)
@@ -178,8 +178,9 @@ def test_decode_layer_step_bf16(H, P, G, gs, batch):
 
 
 def test_decode_layer_step_fp32_and_unfused_agree():
-    """fp32 activations with an fp32 weight, y not requested; against the oracle and
-    against ssd_state_update + gated_rmsnorm run separately."""
+    """fp32 activations with an fp32 weight, y not requested (the norm then runs in place
+    on out); against the oracle and against ssd_state_update + gated_rmsnorm called
+    separately."""
     H, P, G, N, S, gs, batch = 8, 16, 2, 32, 6, 64, 4
     idx = np.array([3, 0, -1, 5], dtype=np.int32)
     u = I.make_update_inputs(S, idx, H, P, G, N, act="f32", seed=451)
