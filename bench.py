@@ -564,9 +564,11 @@ def profile_only(args):
         dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
         return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
 
-    if args.profile in ("scan", "scan_large", "norm", "norm_large"):
-        name = WORKLOAD if args.profile in ("scan", "norm") else "nemotron_h_varlen"
-        s = I.scan_workload(name)
+    if args.profile in ("scan", "scan_large", "scan_split", "norm", "norm_large"):
+        name = WORKLOAD if args.profile in ("scan", "norm", "scan_split") else "nemotron_h_varlen"
+        # scan_split: one 16384-token sequence, which the planner cuts into segments
+        s = (I.scan_workload(name, seqlens=[16384]) if args.profile == "scan_split"
+             else I.scan_workload(name))
         x, dt, A, B, C, Dp, bias, init = (T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D,
                                                             s.dt_bias, s.initial_states))
         hi = torch.from_numpy(s.has_initial_state).to(dev)
@@ -587,12 +589,25 @@ def profile_only(args):
     else:
         # a 96-slot pool (384 MiB, larger than L2) keeps a multi-pass capture small
         H, P, G, N, S, batch = 128, 64, 8, 128, 96, 96
+        if args.profile == "multi":
+            batch = 48
         idx = I.padded_permutation(S, batch, seed=3000 + batch)
+        ntok = 4 if args.profile == "multi" else None
         u = I.make_update_inputs(1, idx, H, P, G, N, act="bf16", seed=3100 + batch,
-                                 pool_values=np.zeros((1, H, P, N), np.float32))
+                                 pool_values=np.zeros((1, H, P, N), np.float32), ntok=ntok)
         pool = torch.randn((S, H, P, N), device=dev, dtype=torch.float32)
         a = (pool, torch.from_numpy(idx).to(dev), T_(u.x), T_(u.dt), T_(u.A), T_(u.B), T_(u.C))
-        run = lambda: ssd.state_update(*a, D=T_(u.D), dt_bias=T_(u.dt_bias))  # noqa
+        if args.profile == "multi":   # 4 tokens per request, per-token states kept
+            inter = torch.empty((batch, 4, H, P, N), device=dev)
+            run = lambda: ssd.state_update_multi(*a, D=T_(u.D), dt_bias=T_(u.dt_bias),  # noqa
+                                                 inter_states=inter)
+        elif args.profile == "copy":  # 32 slots into a snapshot pool
+            snap = torch.empty((32, H, P, N), device=dev)
+            si = torch.arange(0, 64, 2, dtype=torch.int32, device=dev)
+            di = torch.arange(32, dtype=torch.int32, device=dev)
+            run = lambda: ssd.state_copy(pool, si, snap, di)  # noqa
+        else:
+            run = lambda: ssd.state_update(*a, D=T_(u.D), dt_bias=T_(u.dt_bias))  # noqa
     for _ in range(args.warmup + args.steps):
         run()
     torch.cuda.synchronize()
@@ -607,7 +622,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / large-scan legs")
-    ap.add_argument("--profile", choices=["scan", "scan_large", "norm", "norm_large", "update"],
+    ap.add_argument("--profile", choices=["scan", "scan_large", "scan_split", "norm", "norm_large",
+                                          "update", "multi", "copy"],
                     help="only launch this op's benchmark workload steps times (for ncu)")
     args = ap.parse_args()
     if args.profile:
