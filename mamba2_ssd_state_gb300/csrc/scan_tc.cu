@@ -33,7 +33,7 @@
 //               y = Y + 2^cs_i Yoff + D x, then the final state.
 //   warp 14     decay warp: dt (softplus), the base-2 cumulative decay, the column
 //               factors of the mask and the chunk-state weights w, chunks ahead.
-// TMEM: C.B^T (128 columns), M (64), Y x2, S, Yoff x2 (PB each).  Y, Yoff and h^T are
+// TMEM: C.B^T (128 columns), M (64), Y x2, S (x2 for PB <= 32), Yoff x2 (PB each).  Y, Yoff and h^T are
 // double-buffered, so chunk c+1's products run while chunk c's outputs are read; the
 // state chain per chunk is S -> h -> h^T -> Yoff of the next chunk.  Every wait is
 // bounded; a wait that runs out raises a CTA-wide abort flag, every role then drains
@@ -122,19 +122,24 @@ struct Layout {
   static constexpr int kB = 0;                         // NBB x B tile (two [128 x 64] boxes)
   static constexpr int kC = NBB * 32768;               // NBC x C tile
   static constexpr int kX = kC + NBC * 32768;          // NX x x tile
-  static constexpr int kXs = kX + NX * kXPad;          // w o x
-  static constexpr int kHT = kXs + kXPad;              // h^T x 2, [N rows][PB] bf16 each
+  // w o x tiles and S accumulators: two of each where shared and tensor memory allow,
+  // so the mask warps prepare chunk c+1 while S of chunk c still reads its tile
+  static constexpr int NXS = PB <= 32 ? 2 : 1;
+  static constexpr int kXs = kX + NX * kXPad;          // NXS x w o x
+  static constexpr int kHT = kXs + NXS * kXPad;        // h^T x 2, [N rows][PB] bf16 each
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
   static constexpr int kPro = kHT + 2 * kHTPad;        // float [NB][kProStride]
   static constexpr int kBar = kPro + NB * kProStride * 4;
-  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 15;
+  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS;
   static constexpr int kFlags = kBar + kNumBar * 8;    // abort flag, TMEM base
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
   static constexpr int kSwB = PB == 64 ? 3 : PB == 32 ? 2 : 1;  // Swizzle<B,4,3>
   static constexpr uint32_t kSwCode = PB == 64 ? kSw128 : PB == 32 ? kSw64 : kSw32;
   // accumulator columns
-  static constexpr uint32_t kY0 = kColAcc, kS = kColAcc + 2 * PB, kO0 = kColAcc + 3 * PB;
+  static constexpr uint32_t kY0 = kColAcc, kS = kColAcc + 2 * PB, kO0 = kColAcc + (2 + NXS) * PB;
+  static_assert(kO0 + 2 * PB <= 512, "TMEM columns");
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
 };
 
 // softplus for the bf16 path: exp(v) alone below -8 (log1p(e) = e (1 - e/2 ...), relative
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams prm) {
   using L = Layout<PB>;
-  constexpr int NX = L::NX, NBC = L::NBC;
+  constexpr int NX = L::NX, NBC = L::NBC, NXS = L::NXS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
@@ -228,16 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barrier per buffer, so no waiter can fall two phases behind its barrier.
   uint64_t* cb_full = pro_empty + NB;       //       C.B^T in TMEM
   uint64_t* cb_empty = cb_full + 1;         //       C.B^T read (8 mask warps)
-  uint64_t* xs_ready = cb_full + 2;         //       w o x in smem (8 mask warps)
-  uint64_t* s_full = cb_full + 3;           //       S done (also frees w o x)
-  uint64_t* s_empty = cb_full + 4;          //       S read (4 output warps)
-  uint64_t* m_ready = cb_full + 5;          //       M in TMEM (8 mask warps)
-  uint64_t* y_full = cb_full + 6;           // [2]   Y buffer done (also frees M)
-  uint64_t* h_ready = cb_full + 8;          // [2]   h^T buffer written (4 output warps)
-  uint64_t* yoff_full = cb_full + 10;       // [2]   Yoff buffer done
-  uint64_t* y_empty = cb_full + 12;         // [2]   Y and Yoff buffers read (4 output warps)
-  uint64_t* drain = cb_full + 14;           //       teardown: all MMAs retired
-  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 15,
+  uint64_t* xs_ready = cb_full + 2;         // [NXS] w o x in smem (8 mask warps)
+  uint64_t* s_full = xs_ready + NXS;        // [NXS] S done (also frees its w o x tile)
+  uint64_t* s_empty = s_full + NXS;         // [NXS] S read (4 output warps)
+  uint64_t* m_ready = s_empty + NXS;        //       M in TMEM (8 mask warps)
+  uint64_t* y_full = m_ready + 1;           // [2]   Y buffer done (also frees M)
+  uint64_t* h_ready = y_full + 2;           // [2]   h^T buffer written (4 output warps)
+  uint64_t* yoff_full = h_ready + 2;        // [2]   Yoff buffer done
+  uint64_t* y_empty = yoff_full + 2;        // [2]   Y and Yoff buffers read (4 output warps)
+  uint64_t* drain = y_empty + 2;            //       teardown: all MMAs retired
+  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS,
                 "barrier block size must match the barriers laid out here");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
@@ -261,9 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(cb_full, 1);
     mbar_init(cb_empty, kMaskWarps);
-    mbar_init(xs_ready, kMaskWarps);
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, kOutWarps);
+    for (int i = 0; i < NXS; ++i) {
+      mbar_init(&xs_ready[i], kMaskWarps);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kOutWarps);
+    }
     mbar_init(m_ready, kMaskWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&y_full[i], 1);
@@ -447,15 +454,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long t_idle = 0;
       while (ns < nch || ny < nch || nyo < nch) {
         bool progress = false;
-        if (ns < ncb && mbar_test_wait(xs_ready, ns & 1) &&
-            (ns == 0 || mbar_test_wait(s_empty, (ns - 1) & 1))) {
+        // S(k) uses w o x tile and accumulator k % NXS, the ((k / NXS) & 1) phase of their
+        // barriers; the accumulator is free once S(k - NXS) has been read
+        if (ns < ncb && mbar_test_wait(&xs_ready[ns % NXS], (ns / NXS) & 1) &&
+            (ns < NXS || mbar_test_wait(&s_empty[ns % NXS], ((ns / NXS) - 1) & 1))) {
           tc_fence_after();
           // S^T = B^T (w o x): A = B read MN-major, 16 token rows (2 KB) per K step
           const uint64_t da = dB_mn0 + (uint64_t)((ns % NBB) * (32768 >> 4));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + L::kS, da + kk * 128, dXs + kk * L::kXRow, idS, kk > 0);
-          mma_commit(s_full);
+            mma_ss(tmem + L::kS + (ns % NXS) * PB, da + kk * 128,
+                   dXs + (uint64_t)((ns % NXS) * (L::kXPad >> 4)) + kk * L::kXRow, idS, kk > 0);
+          mma_commit(&s_full[ns % NXS]);
           mma_commit(&b_empty[ns % NBB]);
           TRACE(ns, 9);
           ++ns;
@@ -535,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (1) w o x for token row j = r: logical 16-byte chunks of this half at their
       //     swizzled positions (the same in x and in w o x); the buffer is free once the
       //     previous chunk's S product is done
-      if (c >= 1 && !wwait(s_full, (c - 1) & 1)) break;
+      // this chunk's w o x tile was last read by S(c - NXS)
+      if (c >= NXS && !wwait(&s_full[c % NXS], ((c / NXS) - 1) & 1)) break;
       if (warp == 2) TRACE(c, 5);
       {
         const float w = pb[kProW + r];
@@ -550,12 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 f = __bfloat1622float2(e2[e]);
             e2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
           }
-          *reinterpret_cast<uint4*>(sm + L::kXs + off) = xv;
+          *reinterpret_cast<uint4*>(sm + L::kXs + (c % NXS) * L::kXPad + off) = xv;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(xs_ready);
+      if (lane == 0) mbar_arrive(&xs_ready[c % NXS]);
       if (warp == 2) TRACE(c, 14);
       // (2) the decay mask from C.B^T
       if (!wwait(cb_full, c & 1)) break;
@@ -657,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB, sx = c % NX;
       if (!(ok = wwait(&pro_full[b], (c / NB) & 1))) break;
-      if (!(ok = wwait(s_full, c & 1))) break;
+      if (!(ok = wwait(&s_full[c % NXS], (c / NXS) & 1))) break;
       tc_fence_after();
       if (warp == 2 + kMaskWarps) TRACE(c, 7);
       const float* pb = pro + b * kProStride;
@@ -666,13 +677,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int sl = 0; sl < PB / 16; ++sl) {
         float sv[16];
-        tmem_ld16(tmem + lrow + L::kS + 16 * sl, sv);
+        tmem_ld16(tmem + lrow + L::kS + (c % NXS) * PB + 16 * sl, sv);
 #pragma unroll
         for (int e = 0; e < 16; ++e) hreg[16 * sl + e] = fmaf(e_l, hreg[16 * sl + e], sv[e]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
+      if (lane == 0) mbar_arrive(&s_empty[c % NXS]);
       if (c + 1 < nch) write_hT(c & 1);
       if (warp == 2 + kMaskWarps) TRACE(c, 11);
       // then y = Y + 2^cs_i Yoff + D x
