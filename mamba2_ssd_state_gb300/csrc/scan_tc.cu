@@ -762,8 +762,9 @@ namespace {
 //     y_t += 2^{cs'_t} C_t H_k^T,   cs'_t = sum of dt A log2(e) from the segment start to t.
 // The scan kernel leaves L_k and every token's cs'_t (d_k is cs' at the segment's last
 // token) in the workspace.  One fix-up CTA per (later segment, head, channel block) forms
-// H_k from the L_i, adds that term chunk by chunk (tensor core: C H_k^T) and, for the
-// last segment, writes the final state.  It is launched with programmatic stream
+// H_k from the L_i, adds that term chunk by chunk (tensor core: C H_k^T; y tiles in and
+// out by TMA through a three-deep shared ring) and, for the last segment, writes the
+// final state.  It is launched with programmatic stream
 // serialisation: its set-up and its C loads overlap the scan kernel's tail, and it waits
 // for the scan to complete before it reads what the scan wrote.
 
@@ -802,8 +803,11 @@ struct FixLayout {
   static constexpr int kC = 0;                          // 2 x C tile (32 KB each)
   static constexpr int kHT = 65536;                     // H_k^T, [N rows][PB] bf16
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
-  static constexpr int kBar = kHT + kHTPad;
-  static constexpr int kNumBar = 10;
+  static constexpr int kYPad = (QT * kXRow + 1023) / 1024 * 1024;  // a [128 tokens][PB] y tile
+  static constexpr int NY = 3;                                     // y tile ring depth
+  static constexpr int kY = kHT + kHTPad;                          // NY x y tile
+  static constexpr int kBar = kY + NY * kYPad;
+  static constexpr int kNumBar = 10 + 2 * NY;
   static constexpr int kFlags = kBar + kNumBar * 8;
   static constexpr int kSmemBytes = kFlags + 16 + 1024;
   static constexpr int kSwB = PB == 64 ? 3 : PB == 32 ? 2 : 1;
@@ -812,8 +816,9 @@ struct FixLayout {
 };
 
 template <int PB>
-__global__ void __launch_bounds__(kFixThreads, 2)
-    scan_fixup_kernel(const __grid_constant__ CUtensorMap tmC, const FixParams prm) {
+__global__ void __launch_bounds__(kFixThreads, 1)
+    scan_fixup_kernel(const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmY, const FixParams prm) {
   using L = FixLayout<PB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -862,6 +867,9 @@ __global__ void __launch_bounds__(kFixThreads, 2)
   uint64_t* acc_empty = bars + 6;  // [2] read by the 4 epilogue warps
   uint64_t* h_ready = bars + 8;    //     H_k^T in shared memory
   uint64_t* drain = bars + 9;      //     teardown: all MMAs retired
+  constexpr int NY = L::NY;
+  uint64_t* y_full = bars + 10;    // [NY] y tile landed
+  uint64_t* y_free = y_full + NY;  // [NY] y tile written back (its store read the tile)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
   if (threadIdx.x == 0) {
@@ -873,6 +881,10 @@ __global__ void __launch_bounds__(kFixThreads, 2)
     }
     mbar_init(h_ready, 4);
     mbar_init(drain, 1);
+    for (int i = 0; i < NY; ++i) {
+      mbar_init(&y_full[i], 1);
+      mbar_init(&y_free[i], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -889,21 +901,35 @@ __global__ void __launch_bounds__(kFixThreads, 2)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer: C of every chunk
+    // ------------------------------------------------ TMA producer: C and y of every chunk
     if (lane == 0) {
-      int issued = 0;
+      constexpr int kYBytes = QT * L::kXRow;
+      auto load_c = [&](int c) {
+        uint8_t* ct = sm + L::kC + (c & 1) * 32768;
+        mbar_arrive_expect_tx(&c_full[c & 1], 32768);
+        tma_load_3d(ct, &tmC, &c_full[c & 1], 0, gidx, tb + c * QT);
+        tma_load_3d(ct + 16384, &tmC, &c_full[c & 1], 64, gidx, tb + c * QT);
+      };
+      int c_issued = 0, y_issued = 0;
+      for (; c_issued < nch && c_issued < 2; ++c_issued) load_c(c_issued);  // inputs only
+      griddep_wait();  // y below is the scan kernel's output
       for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        if (c >= 2 && !mbar_wait(&c_empty[st], ((c >> 1) - 1) & 1, abort_flag, kWaitLimit)) break;
-        uint8_t* ct = sm + L::kC + st * 32768;
-        mbar_arrive_expect_tx(&c_full[st], 32768);
-        tma_load_3d(ct, &tmC, &c_full[st], 0, gidx, tb + c * QT);
-        tma_load_3d(ct + 16384, &tmC, &c_full[st], 64, gidx, tb + c * QT);
-        TRACE_FIX(1 + c, 3, tr_unit);
-        issued = c + 1;
+        if (c >= 2) {
+          if (!mbar_wait(&c_empty[c & 1], ((c >> 1) - 1) & 1, abort_flag, kWaitLimit)) break;
+          load_c(c);
+          c_issued = c + 1;
+        }
+        if (c >= NY &&
+            !mbar_wait(&y_free[c % NY], ((c / NY) - 1) & 1, abort_flag, kWaitLimit))
+          break;
+        mbar_arrive_expect_tx(&y_full[c % NY], kYBytes);
+        tma_load_3d(sm + L::kY + (c % NY) * L::kYPad, &tmY, &y_full[c % NY], p0, h, tb + c * QT);
+        y_issued = c + 1;
       }
-      for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
+      for (int c = c_issued > 2 ? c_issued - 2 : 0; c < c_issued; ++c)
         mbar_wait_drain(&c_full[c & 1], (c >> 1) & 1, kWaitLimit);
+      for (int c = y_issued > NY ? y_issued - NY : 0; c < y_issued; ++c)
+        mbar_wait_drain(&y_full[c % NY], (c / NY) & 1, kWaitLimit);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer: Yfix = C H_k^T
@@ -982,58 +1008,75 @@ __global__ void __launch_bounds__(kFixThreads, 2)
       for (int k = 0; k < PB; ++k) f[(size_t)k * NSTATE] = hin[k];
     }
     // 2. per chunk: y += 2^{cs'} Yfix, cs' the decay from the segment start to the row's
-    // token.  Row loads run two chunks ahead (two register sets), so a chunk waits on
-    // memory only if the tensor core is faster than two loads in flight.
-    uint4 ya[PB / 8], yb[PB / 8];
-    float csa = 0.f, csb = 0.f;
-    auto load_row = [&](int c, uint4 (&yr)[PB / 8], float& cv) {
+    // token.  The y tile comes in by TMA; each thread updates its row in shared memory;
+    // a full tile goes back by one TMA store, the rows of a sequence's last, partial
+    // tile by plain stores (a tile store would overwrite the next sequence's rows).
+    float csn = 0.f;  // this row's decay for the next chunk, loaded a chunk ahead
+    auto load_cs = [&](int c) {
       const int tok = tb + c * QT + r;
-      if (tok < t1) {
-        const uint4* src = reinterpret_cast<const uint4*>(prm.y + ((size_t)tok * H + h) * P + p0);
-#pragma unroll
-        for (int e = 0; e < PB / 8; ++e) yr[e] = src[e];
-        cv = prm.ws_cs[(size_t)tok * H + h];
-      }
+      csn = tok < t1 ? prm.ws_cs[(size_t)tok * H + h] : 0.f;
     };
-    auto process = [&](int c, uint4 (&yr)[PB / 8], float cv) -> bool {
+    if (nch > 0) load_cs(0);
+    int done_c = 0;
+    for (int c = 0; c < nch; ++c) {
       const int st = c & 1;
       const int tok = tb + c * QT + r;
+      const bool full_tile = tb + (c + 1) * QT <= t1;
+      const float scale = ex2(csn);
+      if (c + 1 < nch) load_cs(c + 1);
       if (r == 0) TRACE_FIX(1 + c, 0, tr_unit);
-      if (!wwait(&acc_full[st], (c >> 1) & 1)) return false;
+      const int sy = c % NY;
+      if (!wwait(&acc_full[st], (c >> 1) & 1) || !wwait(&y_full[sy], (c / NY) & 1)) break;
       if (r == 0) TRACE_FIX(1 + c, 1, tr_unit);
       tc_fence_after();
-      const float scale = ex2(cv);
+      uint8_t* yt = sm + L::kY + sy * L::kYPad;
 #pragma unroll
       for (int sl = 0; sl < PB / 16; ++sl) {
         float fv[16];
         tmem_ld16(tmem + lrow + st * PB + 16 * sl, fv);
-        __nv_bfloat162* y2 = reinterpret_cast<__nv_bfloat162*>(&yr[2 * sl]);
+        uint4* q0 = reinterpret_cast<uint4*>(yt + swz((uint32_t)(r * L::kXRow + 32 * sl), L::kSwB));
+        uint4* q1 =
+            reinterpret_cast<uint4*>(yt + swz((uint32_t)(r * L::kXRow + 32 * sl + 16), L::kSwB));
+        uint4 yv[2] = {*q0, *q1};
+        __nv_bfloat162* y2 = reinterpret_cast<__nv_bfloat162*>(yv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float2 yf = __bfloat1622float2(y2[e]);
           y2[e] = __floats2bfloat162_rn(fmaf(scale, fv[2 * e], yf.x),
                                         fmaf(scale, fv[2 * e + 1], yf.y));
         }
+        if (full_tile) {
+          *q0 = yv[0];
+          *q1 = yv[1];
+        } else if (tok < t1) {
+          uint4* dst = reinterpret_cast<uint4*>(prm.y + ((size_t)tok * H + h) * P + p0 + 16 * sl);
+          dst[0] = yv[0];
+          dst[1] = yv[1];
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[st]);
-      if (tok < t1) {
-        uint4* dst = reinterpret_cast<uint4*>(prm.y + ((size_t)tok * H + h) * P + p0);
-#pragma unroll
-        for (int e = 0; e < PB / 8; ++e) dst[e] = yr[e];
+      if (full_tile) fence_proxy_async_smem();  // the tile store reads what the threads wrote
+      named_bar_sync(1, 128);
+      if (r == 0) {
+        // a tile may be refilled once its store has read it; that wait is deferred by one
+        // chunk (one store group left in flight), so the store overlaps the next chunk
+        if (full_tile) {
+          tma_store_3d(&tmY, yt, p0, h, tb + c * QT);
+          bulk_commit_group();
+        }
+        if (c > 0) {
+          bulk_wait_read_one();
+          mbar_arrive(&y_free[(c - 1) % NY]);
+        }
+        TRACE_FIX(1 + c, 2, tr_unit);
       }
-      if (r == 0) TRACE_FIX(1 + c, 2, tr_unit);
-      return true;
-    };
-    if (nch > 0) load_row(0, ya, csa);
-    if (nch > 1) load_row(1, yb, csb);
-    for (int c = 0; c < nch; c += 2) {
-      if (!process(c, ya, csa)) break;
-      if (c + 2 < nch) load_row(c + 2, ya, csa);
-      if (c + 1 >= nch) break;
-      if (!process(c + 1, yb, csb)) break;
-      if (c + 3 < nch) load_row(c + 3, yb, csb);
+      done_c = c + 1;
+    }
+    if (r == 0) {
+      bulk_wait_all();  // every tile store complete before the kernel ends
+      if (done_c > 0) mbar_arrive(&y_free[(done_c - 1) % NY]);
     }
   }
   __syncthreads();
@@ -1126,10 +1169,10 @@ int min_segc(const ssd_scan_args& a) {
 // lengths live on the device), so sequences are taken as equally long.  One CTA per SM;
 // a CTA of channel block PB that runs n chunks costs about kRamp + n (1 + PB/256) (the
 // mask and C.B^T work does not shrink with PB; kRamp is the pipeline fill of its first
-// chunk).  A split adds the fix-up grid over the later segments, two CTAs per SM: its
-// set-up, one chained step per segment before it (the entering state) and a per-chunk
-// cost close to the scan's own.
-constexpr double kRamp = 3.0, kFixBase = 4.0, kFixPerSeg = 1.0, kFixPerChunk = 1.5;
+// chunk).  A split adds the fix-up grid over the later segments, one CTA per SM: a
+// fixed cost per wave (its launch, set-up and first tile), one chained step per segment
+// before it (the entering state) and about 0.4 of a scan chunk per chunk.
+constexpr double kRamp = 3.0, kFixBase = 7.0, kFixPerSeg = 0.4, kFixPerChunk = 0.4;
 
 double plan_cost(const ssd_scan_args& a, int pb, int segc) {
   const int sms = sm_count();
@@ -1143,7 +1186,7 @@ double plan_cost(const ssd_scan_args& a, int pb, int segc) {
   double cost = (double)waves * (kRamp + chain * (1.0 + pb / 256.0));
   if (nseg > 1) {
     const long long fix_ctas = (long long)a.nseq * (nseg - 1) * per_seg;
-    const long long fix_waves = (fix_ctas + 2 * sms - 1) / (2 * sms);
+    const long long fix_waves = (fix_ctas + sms - 1) / sms;
     cost += fix_waves * (kFixBase + kFixPerSeg * nseg + kFixPerChunk * chain);
   }
   return cost;
@@ -1275,7 +1318,11 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, scan_fixup_kernel<PB>, mC, fp) != cudaSuccess) return SSD_ERR_CUDA;
+  CUtensorMap mY;  // y as the fix-up reads and writes it: tiles of [128 tokens][PB channels]
+  if (!make_map(&mY, a.y, a.P, a.H, T, (uint64_t)a.P * 2, (uint64_t)a.H * a.P * 2, PB, QT, xsw))
+    return SSD_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, scan_fixup_kernel<PB>, mC, mY, fp) != cudaSuccess)
+    return SSD_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
