@@ -9,6 +9,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+
 from mamba2_ssd_state_gb300 import inputs as I
 from mamba2_ssd_state_gb300 import ssd
 from gpu_util import dev, scan_gpu, scan_oracle
@@ -250,3 +252,67 @@ def test_single_long_sequence_planned_split():
     y1, f1, _ = scan_gpu(s, seg_chunks=-1)
     check_bf16("single 16384 split vs unsplit y", y, y1)
     check_bf16("single 16384 split vs unsplit final", fs, f1)
+
+
+# ----------------------------------------------------------------------- more edge shapes
+
+def test_many_short_sequences_tc():
+    """300 packed sequences of 0 to 40 tokens (a third of them empty or one token), mixed
+    initial states: 300 chains of one partial chunk each."""
+    rng = np.random.default_rng(501)
+    lens = rng.integers(0, 41, 300)
+    lens[::7] = 0
+    lens[::11] = 1
+    init = (rng.random(300) < 0.5).astype(int).tolist()
+    s = I.make_scan_inputs(lens.tolist(), H=2, P=32, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=503, init=init)
+    y, fs, bits = scan_gpu(s, impl="tc")
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("300 short seqs y", y, yr)
+    check_bf16("300 short seqs final", fs, fr)
+    empty = np.flatnonzero(lens == 0)
+    np.testing.assert_array_equal(fs[empty], s.initial_states.values[empty])
+
+
+def test_tc_headdim_128_group_per_head():
+    """P = 128 (two 64-channel blocks per head), G = H: every head its own B and C."""
+    s = I.make_scan_inputs([300, 77, 513], H=3, P=128, G=3, N=128, chunk_size=128, act="bf16",
+                           seed=507, init=[1, 1, 0])
+    for pb in (64, 32):
+        y, fs, bits = scan_gpu(s, impl="tc", p_block=pb)
+        assert bits == 0
+        yr, fr = scan_oracle(s)
+        check_bf16(f"P=128 pb={pb} y", y, yr)
+        check_bf16(f"P=128 pb={pb} final", fs, fr)
+
+
+def test_tc_plain_dt_no_D_all_initial():
+    """dt used as given (no softplus, no bias: positive raw values), no D, initial states
+    for every sequence with has_initial_state left NULL (all used)."""
+    s = I.make_scan_inputs([250, 129, 1], H=4, P=64, G=2, N=128, chunk_size=128, act="bf16",
+                           seed=509, init="all")
+    s.dt = I.Tensor(np.abs(s.dt.values) * 0.05 + 0.01, "f32")
+    cu = torch.from_numpy(s.cu_seqlens).cuda()
+    status = ssd.new_status()
+    y, fs = ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C), cu_seqlens=cu,
+                           chunk_size=128, dt_softplus=False,
+                           initial_states=dev(s.initial_states), status=status, impl="tc")
+    assert ssd.read_status(status)[1] == 0
+    yr, fr = oracle.scan_seq(s.x.values, s.dt.values, s.A.values, s.B.values, s.C.values,
+                             dt_softplus=False,
+                             initial_states=s.initial_states.values, cu_seqlens=s.cu_seqlens)
+    check_bf16("plain dt y", y.float().cpu().numpy(), yr)
+    check_bf16("plain dt final", fs.cpu().numpy(), fr)
+
+
+def test_split_instance_without_split_sequences():
+    """A forced segment length longer than every sequence: the segmented kernel instance
+    runs, but no sequence has a second segment, so no fix-up CTA has work."""
+    s = I.make_scan_inputs([300, 5, 0, 250], H=2, P=64, G=1, N=128, chunk_size=256,
+                           act="bf16", seed=511, init=[1, 0, 1, 1])
+    y, fs, bits = scan_gpu(s, impl="tc", seg_chunks=8)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("no-split instance y", y, yr)
+    check_bf16("no-split instance final", fs, fr)
