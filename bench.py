@@ -212,11 +212,11 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[3].record(stream)
 
-    # the scan is one launch, or three when the library splits the two sequences into
-    # segments (scan, combine, fix-up)
+    # the scan is one launch, or two when the library splits the sequences into segments
+    # (scan, fix-up)
     scan_split = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu,
                                                chunk_size=s.chunk_size) > 0
-    launches_per_step = (3 if scan_split else 1) + 2
+    launches_per_step = (2 if scan_split else 1) + 2
     for i in range(max(args.warmup, 3)):
         l2.flush()
         step()
@@ -227,7 +227,13 @@ def run_ours(args, rank, world, local_rank):
     if bits:
         raise RuntimeError(f"device status bits {bits} after warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # The timed step is one CUDA graph of its launches (the way a serving engine runs a
+    # layer): no host work and no launch gaps between the scan, the norm and the decode.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     # the timed region is milliseconds long: keep the GPU under the same load for a
@@ -236,7 +242,7 @@ def run_ours(args, rank, world, local_rank):
     while time.perf_counter() - t_load < 1.0:
         for _ in range(50):
             l2.flush()
-            step()
+            graph.replay()
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -244,17 +250,26 @@ def run_ours(args, rank, world, local_rank):
     t_wall0 = time.perf_counter()
     for k in range(args.steps):
         l2.flush()             # outside the step's events
-        step(evs[k])
+        evs[k][0].record(stream)
+        graph.replay()
+        evs[k][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
     ck = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    scan_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    norm_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    upd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = shard.max_over_ranks(sum(step_ms), dev)
+    # per-op split of a step: the same step launched op by op, events between the ops
+    # (not part of `value`; launch gaps make these slightly longer than inside the graph)
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        l2.flush()
+        step(evb[k])
+    torch.cuda.synchronize()
+    scan_ms = [e[0].elapsed_time(e[1]) for e in evb]
+    norm_ms = [e[1].elapsed_time(e[2]) for e in evb]
+    upd_ms = [e[2].elapsed_time(e[3]) for e in evb]
     tokens_per_step = T + nseq
     value = tokens_per_step * world * args.steps / (total_ms / 1e3)
 
@@ -355,6 +370,7 @@ def run_ours(args, rank, world, local_rank):
                                "both requests", "seqlens": s.seqlens, "H": H, "P": P, "G": G,
                    "N": N, "chunk_size": s.chunk_size, "tokens_per_step": tokens_per_step,
                    "l2": L2Flush.DESCRIPTION,
+                   "launch": "the step's kernels replayed as one CUDA graph",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "breakdown_us": {"scan": scan_avg * 1e3, "gated_rmsnorm": 1e3 * sum(norm_ms) / len(norm_ms),
                          "state_update": 1e3 * sum(upd_ms) / len(upd_ms)},
