@@ -57,6 +57,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "scan_segments.cuh"
@@ -1117,17 +1118,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices ? dev : 0;
+}
+
+// SM count of the current device, looked up once per device (148 if it cannot be read).
 int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      sms = n;
-    else
-      sms = 148;
+  static std::atomic<int> sms[kMaxDevices];
+  const int dev = current_device();
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  return sms;
+  return n;
 }
 
 // How one call runs: channel block PB, segment length segc (0 = sequences are not split),
@@ -1247,8 +1255,10 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
       !make_map(&mC, a.C, NSTATE, a.G, T, NSTATE * 2, (uint64_t)cs * 2, 64, QT,
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return SSD_ERR_CUDA;
-  static bool attr_set = false;  // per template instance
-  if (!attr_set) {
+  // dynamic shared memory above 48 KB is opted into once per kernel and device
+  static std::atomic<bool> attr_set[kMaxDevices];
+  const int dev = current_device();
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(scan_tc_kernel<PB, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kSmemBytes) != cudaSuccess ||
@@ -1258,7 +1268,7 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
         cudaFuncSetAttribute(scan_fixup_kernel<PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              FixLayout<PB>::kSmemBytes) != cudaSuccess)
       return SSD_ERR_CUDA;
-    attr_set = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const bool split = plan.segc > 0;
   float* ws_h = split ? static_cast<float*>(a.workspace) : nullptr;
