@@ -19,11 +19,14 @@
  * Conventions shared by every entry point:
  *   - Every pointer argument is DEVICE memory owned by the caller, except the args
  *     structs themselves (host).  The library keeps no pointer after it returns and
- *     allocates no memory; the one scratch buffer (the scan's optional workspace) is
- *     the caller's too.
+ *     allocates no memory when called; the one scratch buffer (the scan's optional
+ *     workspace) is the caller's too (ssd_chunk_scan_static_ws instead uses a 16 MiB
+ *     array that is part of the library's image).
  *   - Every call is asynchronous on the caller's stream (a cudaStream_t passed as
  *     ssd_stream_t; NULL = the legacy default stream).  Nothing is copied device to
- *     host and no call synchronises, except ssd_read_status.
+ *     host and no call synchronises, except ssd_read_status.  ssd_chunk_scan,
+ *     gated_rmsnorm and the decode calls only launch kernels on that stream, so a
+ *     sequence of them can be captured into a CUDA graph and replayed.
  *   - Errors the host can see (NULL required pointer, bad size, unsupported dtype or
  *     shape) are returned before anything is launched.  Errors only the device can
  *     see (A not negative, slot index out of range, malformed cu_seqlens) are OR-ed as
