@@ -36,11 +36,4 @@ __device__ inline bool find_segment(const int32_t* cu, int nseq, int segc, int j
   return false;
 }
 
-// Index of the first segment of sequence s.
-__device__ inline int first_segment(const int32_t* cu, int s, int segc) {
-  int off = 0;
-  for (int i = 0; i < s; ++i) off += seg_count(cu[i + 1] - cu[i], segc);
-  return off;
-}
-
 }  // namespace ssd
