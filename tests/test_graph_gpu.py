@@ -1,7 +1,7 @@
 """The library's calls are asynchronous on the caller's stream and capturable: a CUDA graph
 of one layer step (a split scan, whose fix-up kernel is launched with programmatic
-dependent launch, then the gated norm and a decode update) replays to the same results
-as the calls made eagerly."""
+dependent launch, then the gated norm, with a decode update on a second stream forked
+and joined inside the capture) replays to the same results as the calls made eagerly."""
 import numpy as np
 import pytest
 import torch
@@ -28,11 +28,18 @@ def test_layer_step_in_a_cuda_graph_matches_eager():
                      device="cuda")
     assert ws.numel() > 0
 
+    side = torch.cuda.Stream()
+
     def run(y, fs, out, pool, uy):
+        # the decode token forks onto a second stream and joins at the end
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            ssd.state_update(pool, idx, ux, udt, uA, uB, uC, D=uD, dt_bias=ubias, y=uy)
         ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=256, D=D, dt_bias=bias,
                        initial_states=init, y=y, final_states=fs, seg_chunks=4, workspace=ws)
         ssd.gated_rmsnorm(y.view(T, d), z, w, group_size=1536, out=out)
-        ssd.state_update(pool, idx, ux, udt, uA, uB, uC, D=uD, dt_bias=ubias, y=uy)
+        main.wait_stream(side)
 
     idx = torch.tensor([2, 0], dtype=torch.int32, device="cuda")
     ux, udt, uA, uB, uC, uD, ubias = (dev(t) for t in (u.x, u.dt, u.A, u.B, u.C, u.D,
