@@ -78,7 +78,17 @@ constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
 constexpr int kThreads = 32 * (kDecayWarp + 1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFactorLimit = 64.f;            // log2 bound of a factorised decay factor
-constexpr long long kWaitLimit = 4000000000LL;  // SM cycles (about 2 s)
+#ifndef SSD_WAIT_LIMIT_CYCLES
+#define SSD_WAIT_LIMIT_CYCLES 4000000000LL  // about 2 s
+#endif
+constexpr long long kWaitLimit = SSD_WAIT_LIMIT_CYCLES;  // SM cycles a wait may take
+
+#ifdef SSD_FAULT_INJECT
+// Test builds only: the decay warp of every CTA withholds the "decay ready" arrival of
+// this chunk (-1 = none), so every role's bounded wait runs out and the kernel must
+// abort cleanly with SSD_DEV_TIMEOUT.
+__device__ int g_inject_withhold_chunk = -1;
+#endif
 
 // TMEM columns (fp32 unless noted)
 constexpr uint32_t kColCB = 0;    // C.B^T, 128 columns
@@ -423,7 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pb[kProSafe + k] = (span <= kFactorLimit && blk_max[k] - anchor <= kFactorLimit) ? 1.f : 0.f;
       }
       __syncwarp();
+#ifdef SSD_FAULT_INJECT
+      if (lane == 0 && c != g_inject_withhold_chunk) mbar_arrive(&pro_full[b]);
+#else
       if (lane == 0) mbar_arrive(&pro_full[b]);
+#endif
       TRACE(c, 2);
     }
   } else if (warp == 1) {
@@ -753,6 +767,14 @@ extern "C" SSD_API int ssd_trace_read(long long* dst) {
 namespace {
 #endif
 
+
+#ifdef SSD_FAULT_INJECT
+}  // namespace
+extern "C" SSD_API int ssd_test_withhold_chunk(int chunk) {
+  return (int)cudaMemcpyToSymbol(g_inject_withhold_chunk, &chunk, sizeof(int));
+}
+namespace {
+#endif
 // ------------------------------------------------------------------ split sequences
 //
 // When a sequence is split into segments, segment k > 0 was scanned from a zero state and
@@ -1027,12 +1049,16 @@ __global__ void __launch_bounds__(kFixThreads, 1)
       if (c + 1 < nch) load_cs(c + 1);
       if (r == 0) TRACE_FIX(1 + c, 0, tr_unit);
       const int sy = c % NY;
-      if (!wwait(&acc_full[st], (c >> 1) & 1) || !wwait(&y_full[sy], (c / NY) & 1)) break;
+      // A wait that fails (an abort) skips this chunk's work, but every epilogue warp still
+      // reaches the named barrier below, which ORs the failures, so they all leave the
+      // loop there together: a warp leaving early would strand the others in the barrier.
+      const bool ok = wwait(&acc_full[st], (c >> 1) & 1) && wwait(&y_full[sy], (c / NY) & 1);
       if (r == 0) TRACE_FIX(1 + c, 1, tr_unit);
       tc_fence_after();
       uint8_t* yt = sm + L::kY + sy * L::kYPad;
 #pragma unroll
       for (int sl = 0; sl < PB / 16; ++sl) {
+        if (!ok) break;
         float fv[16];
         tmem_ld16(tmem + lrow + st * PB + 16 * sl, fv);
         uint4* q0 = reinterpret_cast<uint4*>(yt + swz((uint32_t)(r * L::kXRow + 32 * sl), L::kSwB));
@@ -1057,9 +1083,9 @@ __global__ void __launch_bounds__(kFixThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[st]);
+      if (ok && lane == 0) mbar_arrive(&acc_empty[st]);
       if (full_tile) fence_proxy_async_smem();  // the tile store reads what the threads wrote
-      named_bar_sync(1, 128);
+      if (named_bar_sync_or(1, 128, !ok)) break;  // the same decision in every epilogue warp
       if (r == 0) {
         // a tile may be refilled once its store has read it; that wait is deferred by one
         // chunk (one store group left in flight), so the store overlaps the next chunk

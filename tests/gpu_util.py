@@ -1,5 +1,7 @@
 """Helpers shared by the GPU parity tests: move seeded inputs to the device, run the
 library through its binding, and run the oracle on the same values."""
+import ctypes
+
 import numpy as np
 import torch
 
@@ -48,3 +50,26 @@ def scan_oracle(s, heads=None, with_abs=False, D=True):
     return oracle.scan_seq(x, dt, A, B, C, D=Dv if D else None, dt_bias=bias,
                            initial_states=init, has_initial_state=s.has_initial_state,
                            cu_seqlens=s.cu_seqlens, with_abs=with_abs)
+
+
+def scan_args_struct(x, dt, A, B, C, cu, chunk_size, *, D=None, dt_bias=None, init=None, y=None,
+          fs=None, status=None, seg_chunks=0):
+    """ssd_scan_args for the given tensors (the marshalling of ssd.chunk_scan), for tests
+    that call an entry point of the C ABI directly."""
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    a = ssd.ScanArgs()
+    a.struct_size = ctypes.sizeof(ssd.ScanArgs)
+    a.x, a.x_stride_t = ssd._ptr(x), H * P
+    a.dt, a.dt_bias, a.dt_softplus = ssd._ptr(dt), ssd._ptr(dt_bias), 1
+    a.A, a.D = ssd._ptr(A), ssd._ptr(D)
+    a.B, a.B_stride_t = ssd._ptr(B), G * N
+    a.C, a.C_stride_t = ssd._ptr(C), G * N
+    a.initial_states = ssd._ptr(init)
+    a.cu_seqlens = ssd._ptr(cu)
+    a.nseq, a.T, a.H, a.P, a.G, a.N = cu.shape[0] - 1, T, H, P, G, N
+    a.chunk_size = chunk_size
+    a.act_dtype = ssd._act(x)
+    a.y, a.final_states, a.d_status = ssd._ptr(y), ssd._ptr(fs), ssd._ptr(status)
+    a.seg_chunks = seg_chunks
+    return a

@@ -14,31 +14,10 @@ import torch
 
 from mamba2_ssd_state_gb300 import inputs as I
 from mamba2_ssd_state_gb300 import ssd
+from gpu_util import scan_args_struct as _args
 from tolerance import check_bf16
 
 SCRATCH_BYTES = 16 << 20
-
-
-def _args(x, dt, A, B, C, cu, chunk_size, *, D=None, dt_bias=None, init=None, y=None,
-          fs=None, status=None, seg_chunks=0):
-    """ssd_scan_args for the given tensors (same marshalling as ssd.chunk_scan)."""
-    T, H, P = x.shape
-    G, N = B.shape[1], B.shape[2]
-    a = ssd.ScanArgs()
-    a.struct_size = ctypes.sizeof(ssd.ScanArgs)
-    a.x, a.x_stride_t = ssd._ptr(x), H * P
-    a.dt, a.dt_bias, a.dt_softplus = ssd._ptr(dt), ssd._ptr(dt_bias), 1
-    a.A, a.D = ssd._ptr(A), ssd._ptr(D)
-    a.B, a.B_stride_t = ssd._ptr(B), G * N
-    a.C, a.C_stride_t = ssd._ptr(C), G * N
-    a.initial_states = ssd._ptr(init)
-    a.cu_seqlens = ssd._ptr(cu)
-    a.nseq, a.T, a.H, a.P, a.G, a.N = cu.shape[0] - 1, T, H, P, G, N
-    a.chunk_size = chunk_size
-    a.act_dtype = ssd._act(x)
-    a.y, a.final_states, a.d_status = ssd._ptr(y), ssd._ptr(fs), ssd._ptr(status)
-    a.seg_chunks = seg_chunks
-    return a
 
 
 def test_static_ws_rejects_oversize_plans_and_caller_workspace():
