@@ -25,8 +25,9 @@
  *   - Every call is asynchronous on the caller's stream (a cudaStream_t passed as
  *     ssd_stream_t; NULL = the legacy default stream).  Nothing is copied device to
  *     host and no call synchronises, except ssd_read_status.  ssd_chunk_scan,
- *     gated_rmsnorm and the decode calls only launch kernels on that stream, so a
- *     sequence of them can be captured into a CUDA graph and replayed.
+ *     ssd_chunk_scan_gated_norm, gated_rmsnorm and the decode calls only launch kernels
+ *     on that stream, so a sequence of them can be captured into a CUDA graph and
+ *     replayed.
  *   - Errors the host can see (NULL required pointer, bad size, unsupported dtype or
  *     shape) are returned before anything is launched.  Errors only the device can
  *     see (A not negative, slot index out of range, malformed cu_seqlens) are OR-ed as
@@ -191,6 +192,33 @@ SSD_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args);
  * Never allocates (no cudaMalloc, no allocating library routine); never synchronises.
  * ------------------------------------------------------------------------------------ */
 SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_chunk_scan_gated_norm -- the prefill half of a Mamba2 mixer after its projections:
+ * the chunked scan with D skip of ssd_chunk_scan, then the silu-gated RMSNorm of
+ * gated_rmsnorm over its output (the layer order scan, D skip, gated RMSNorm of the
+ * Nemotron-H layer path; vt::RmsNormGatedGroup of [vllm.cpp #566]), in one call.
+ *
+ * The two run as kernels back to back on the stream; the norm is launched as a
+ * programmatic dependent of the scan.  Its blocks take the SMs the scan leaves idle
+ * and load z and the weights while the scan runs, then wait for the scan to complete
+ * (griddepcontrol.wait) before they read y, which is still in L2.  The tensor-core scan
+ * kernels signal their dependents early (griddepcontrol.launch_dependents): a kernel a
+ * caller launches after ssd_chunk_scan with programmatic stream serialisation must
+ * likewise wait (cudaGridDependencySynchronize) before it reads the scan's outputs.
+ *
+ * Arguments: args as ssd_chunk_scan, except that args->y may be NULL (then y is written
+ * into out and normalised in place); z [T, H*P] act_dtype or NULL (no gate), which must
+ * share no byte with y or out (else SSD_ERR_INVALID_ARG) and must not be written by the
+ * scan; norm_weight [H*P] weight_dtype; out [T, H*P] act_dtype, may be args->y.
+ * group_size: channels per norm group, dividing H*P.  eps >= 0.  Errors are those of
+ * ssd_chunk_scan and gated_rmsnorm, all returned before any launch.  With T == 0 only
+ * the final states are written.
+ * ------------------------------------------------------------------------------------ */
+SSD_API ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const void* z,
+                                             const void* norm_weight, ssd_dtype weight_dtype,
+                                             int32_t group_size, float eps, void* out,
+                                             ssd_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * ssd_state_update -- one decode token per request on a pooled state cache,

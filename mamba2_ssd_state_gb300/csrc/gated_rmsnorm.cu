@@ -8,7 +8,13 @@
 // One warp owns one (row, group); in the vector path every lane keeps its
 // VPT * 8 gated values in registers between the reduction and the write, so the op is a
 // single pass over memory with 16-byte loads and stores and a warp-shuffle reduction.
+//
+// Launched as a programmatic dependent of the scan (the scan + norm call), a block may
+// start while the scan is still running: it loads z, an input of the whole call, then
+// waits (griddepcontrol.wait) for the scan to complete before it reads x, the scan's y.
+// Launched plainly, the wait returns at once.
 #include "ssd_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace ssd {
 namespace {
@@ -92,23 +98,22 @@ __global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
   const size_t base = (size_t)row * d + col0;
   float g[VPT][8];
   float ss = 0.f;
+  if (valid && z) {  // z first: it may be read before the producer of x has finished
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) Vec8<TA>::load(z + base + 8 * (tig + TPG * i), g[i]);
+  }
+  tc::griddep_wait();
   if (valid) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int off = 8 * (tig + TPG * i);
       float xv[8];
       Vec8<TA>::load(x + base + off, xv);
-      if (z) {
-        float zv[8];
-        Vec8<TA>::load(z + base + off, zv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) g[i][e] = xv[e] * gate<TA>(zv[e]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) g[i][e] = xv[e];
+      for (int e = 0; e < 8; ++e) {
+        g[i][e] = z ? xv[e] * gate<TA>(g[i][e]) : xv[e];
+        ss = fmaf(g[i][e], g[i][e], ss);
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(g[i][e], g[i][e], ss);
     }
   }
   ss = warp_sum(ss);
@@ -142,6 +147,7 @@ __global__ void __launch_bounds__(256) norm_generic_kernel(const TA* x,
                                                            const TW* __restrict__ w, TA* out,
                                                            int64_t units, int d, int gs,
                                                            float eps) {
+  tc::griddep_wait();  // x may be the output of the kernel before (see norm_vec_kernel)
   const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (unit >= units) return;
   const int lane = threadIdx.x & 31;
@@ -164,9 +170,26 @@ __global__ void __launch_bounds__(256) norm_generic_kernel(const TA* x,
   }
 }
 
+// 256-thread blocks on `st`; with pdl the launch may begin before the previous kernel on
+// the stream has completed (programmatic stream serialisation).
+template <typename... P, typename... A>
+cudaError_t launch256(void (*kernel)(P...), int64_t blocks, bool pdl, cudaStream_t st,
+                      A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <typename TA, typename TW>
 cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out, int64_t rows,
-                         int d, int gs, float eps, cudaStream_t st) {
+                         int d, int gs, float eps, bool pdl, cudaStream_t st) {
   const int64_t units = rows * (int64_t)(d / gs);
   const int64_t blocks = (units + 7) / 8;
   const TA* xp = static_cast<const TA*>(x);
@@ -190,32 +213,30 @@ cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out,
   }
   const int gpb = tpg ? 256 / tpg : 8;
   const int64_t vblocks = (units + gpb - 1) / gpb;
-#define SSD_NORM_CASE(V, T)                                                               \
-  if (vpt == V && tpg == T) {                                                              \
-    norm_vec_kernel<TA, TW, V, T><<<(unsigned)vblocks, 256, 0, st>>>(xp, zp, wp, op, units, \
-                                                                     d, gs, eps);           \
-    return cudaGetLastError();                                                             \
-  }
+#define SSD_NORM_CASE(V, T)                                                                 \
+  if (vpt == V && tpg == T)                                                                  \
+    return launch256(norm_vec_kernel<TA, TW, V, T>, vblocks, pdl, st, xp, zp, wp, op, units, d, \
+                     gs, eps);
   SSD_NORM_CASE(1, 32) SSD_NORM_CASE(2, 32) SSD_NORM_CASE(3, 32) SSD_NORM_CASE(4, 32)
   SSD_NORM_CASE(3, 64) SSD_NORM_CASE(4, 64) SSD_NORM_CASE(3, 128) SSD_NORM_CASE(4, 128)
   SSD_NORM_CASE(3, 256) SSD_NORM_CASE(4, 256)
 #undef SSD_NORM_CASE
-  norm_generic_kernel<TA, TW><<<(unsigned)blocks, 256, 0, st>>>(xp, zp, wp, op, units, d, gs, eps);
-  return cudaGetLastError();
+  return launch256(norm_generic_kernel<TA, TW>, blocks, pdl, st, xp, zp, wp, op, units, d, gs,
+                   eps);
 }
 
 }  // namespace
 
 cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, void* out,
                                  int64_t rows, int d, int gs, float eps, ssd_dtype act,
-                                 ssd_dtype wt, cudaStream_t st) {
+                                 ssd_dtype wt, cudaStream_t st, bool pdl) {
   if (rows == 0) return cudaSuccess;
+  using bf = __nv_bfloat16;
   if (act == SSD_BF16)
-    return wt == SSD_BF16
-               ? launch_typed<__nv_bfloat16, __nv_bfloat16>(x, z, w, out, rows, d, gs, eps, st)
-               : launch_typed<__nv_bfloat16, float>(x, z, w, out, rows, d, gs, eps, st);
-  return wt == SSD_BF16 ? launch_typed<float, __nv_bfloat16>(x, z, w, out, rows, d, gs, eps, st)
-                        : launch_typed<float, float>(x, z, w, out, rows, d, gs, eps, st);
+    return wt == SSD_BF16 ? launch_typed<bf, bf>(x, z, w, out, rows, d, gs, eps, pdl, st)
+                          : launch_typed<bf, float>(x, z, w, out, rows, d, gs, eps, pdl, st);
+  return wt == SSD_BF16 ? launch_typed<float, bf>(x, z, w, out, rows, d, gs, eps, pdl, st)
+                        : launch_typed<float, float>(x, z, w, out, rows, d, gs, eps, pdl, st);
 }
 
 }  // namespace ssd

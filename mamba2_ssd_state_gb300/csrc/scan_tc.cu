@@ -306,9 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // the fix-up kernel (split sequences) may be scheduled once every CTA holds its tensor
-  // memory; it waits for this grid to complete before it reads what this grid writes
-  if (kSplit && threadIdx.x == 0) griddep_launch_dependents();
+  // a programmatic dependent (the fix-up kernel of split sequences, the norm of the
+  // scan + norm call) may be scheduled once every CTA holds its tensor memory; it waits
+  // for this grid to complete before it reads anything this grid writes
+  if (threadIdx.x == 0) griddep_launch_dependents();
   auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
     return warp_wait(bar, par, abort_flag, kWaitLimit);
   };
@@ -919,6 +920,9 @@ __global__ void __launch_bounds__(kFixThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // a programmatic dependent (the norm of the scan + norm call) may be scheduled now; it
+  // waits for this grid, and so for the scan kernel before it, to complete
+  if (threadIdx.x == 0) griddep_launch_dependents();
   auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
     return warp_wait(bar, par, abort_flag, kWaitLimit);
   };

@@ -89,6 +89,37 @@ ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_stream_t stre
   return launch_scan_simt(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const void* z,
+                                     const void* norm_weight, ssd_dtype weight_dtype,
+                                     int32_t group_size, float eps, void* out,
+                                     ssd_stream_t stream) {
+  if (!args || args->struct_size < sizeof(ssd_scan_args)) return SSD_ERR_INVALID_ARG;
+  ssd_scan_args a = *args;  // y is optional here: the scan then writes into out
+  if (!a.y) a.y = out;
+  ssd_status v = validate_scan(&a);
+  if (v != SSD_OK) return v;
+  const int64_t d = (int64_t)a.H * a.P;
+  if (!norm_weight || bad_dtype(weight_dtype) || !(eps >= 0.f)) return SSD_ERR_INVALID_ARG;
+  if (group_size < 1 || d % group_size != 0) return SSD_ERR_INVALID_ARG;
+  if (d > 0x7fffffffLL || ((int64_t)a.T * (d / group_size) + 7) / 8 > 0x7fffffffLL)
+    return SSD_ERR_UNSUPPORTED;  // grid limits of the norm
+  if (a.T == 0) return ssd_chunk_scan(&a, stream);  // final states only
+  // the norm may read z while the scan still runs: z must not share bytes with y or out
+  const size_t bytes = (size_t)a.T * (size_t)d * (a.act_dtype == SSD_BF16 ? 2 : 4);
+  auto overlap = [bytes](const void* p, const void* q) {
+    const uintptr_t u = (uintptr_t)p, w = (uintptr_t)q;
+    return u < w + bytes && w < u + bytes;
+  };
+  if (z && (overlap(z, a.y) || overlap(z, out))) return SSD_ERR_INVALID_ARG;
+  v = ssd_chunk_scan(&a, stream);
+  if (v != SSD_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_gated_rmsnorm(a.y, z, norm_weight, out, a.T, (int)d, group_size, eps,
+                              a.act_dtype, weight_dtype, st, /*pdl=*/true) == cudaSuccess
+             ? SSD_OK
+             : SSD_ERR_CUDA;
+}
+
 size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args) {
   if (validate_scan(args) != SSD_OK) return 0;
   const ssd_scan_args& a = *args;

@@ -31,9 +31,11 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bit) {
 
 // Launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_state_update(const ssd_update_args& a, cudaStream_t s);
+// pdl: launch as a programmatic dependent of the previous kernel on the stream (which
+// must not write z or w; the kernel waits for it before reading x).
 cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, void* out,
                                  int64_t rows, int d, int gs, float eps, ssd_dtype act,
-                                 ssd_dtype wt, cudaStream_t s);
+                                 ssd_dtype wt, cudaStream_t s, bool pdl = false);
 cudaError_t launch_scan_simt(const ssd_scan_args& a, cudaStream_t s);
 
 // Tensor-core scan: supported shapes, the workspace its plan wants (0 = no split) and the

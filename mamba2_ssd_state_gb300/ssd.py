@@ -71,6 +71,9 @@ def load_library(path: str | None = None):
         lib.ssd_chunk_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssd_chunk_scan_static_ws.argtypes = [ctypes.POINTER(ScanArgs), _vp]
         lib.ssd_chunk_scan_static_ws.restype = ctypes.c_int
+        lib.ssd_chunk_scan_gated_norm.argtypes = [ctypes.POINTER(ScanArgs), _vp, _vp,
+                                                  ctypes.c_int, _i32, ctypes.c_float, _vp, _vp]
+        lib.ssd_chunk_scan_gated_norm.restype = ctypes.c_int
         lib.ssd_state_update_multi.argtypes = [ctypes.POINTER(UpdateArgs), _i32, _vp, _vp]
         lib.ssd_state_update_multi.restype = ctypes.c_int
         lib.ssd_decode_layer_step.argtypes = [ctypes.POINTER(UpdateArgs), _vp, _vp, ctypes.c_int,
@@ -129,6 +132,8 @@ def _token_stride(t, name, inner):
     """Token (first-dim) stride in elements; the inner dims must be dense."""
     if t.dim() < 2:
         raise ValueError(f"{name} must be at least 2-D")
+    if t.numel() == 0:
+        return int(inner)  # no element is addressed: any strides will do
     exp = 1
     for d in range(t.dim() - 1, 0, -1):
         if t.stride(d) != exp:
@@ -162,6 +167,52 @@ def chunk_scan(x, dt, A, B, C, *, cu_seqlens, chunk_size, D=None, dt_bias=None,
     sequences (it then gets a workspace from torch's allocator unless one is passed),
     -1 = never, k >= 1 = segments of k 128-token chunks.  Returns (y, final_states)."""
     lib = load_library()
+    a, y, final_states, _ws = _scan_args(
+        lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus, initial_states,
+        has_initial_state, y, final_states, return_final_states, status, impl, p_block,
+        seg_chunks, workspace)
+    _raise(lib.ssd_chunk_scan(ctypes.byref(a), _stream(stream)), "ssd_chunk_scan")
+    return y, final_states
+
+
+def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_size,
+                          group_size, eps=1e-5, D=None, dt_bias=None, dt_softplus=True,
+                          initial_states=None, has_initial_state=None, y=None, out=None,
+                          final_states=None, return_final_states=True, status=None,
+                          impl="auto", p_block=0, seg_chunks=0, workspace=None, stream=None):
+    """The scan of chunk_scan followed by the gated RMSNorm of gated_rmsnorm over its
+    output, in one call (ssd_chunk_scan_gated_norm in ssd.h).  z [T,H*P] (or None: no
+    gate), norm_weight [H*P].  y (optional) receives the pre-norm output; without it the
+    scan writes into out.  Returns (out [T,H*P], final_states)."""
+    lib = load_library()
+    T, H, P = x.shape
+    dev = x.device
+    _check(z, "z", x.dtype, (T, H * P), dev)
+    _check(norm_weight, "norm_weight", None, (H * P,), dev)
+    for t, nm in ((z, "z"), (norm_weight, "norm_weight")):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    if out is None:
+        out = torch.empty((T, H * P), dtype=x.dtype, device=dev)
+    _check(out, "out", x.dtype, (T, H * P), dev)
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    a, y, final_states, _ws = _scan_args(
+        lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus, initial_states,
+        has_initial_state, y if y is not None else out.view(T, H, P), final_states,
+        return_final_states, status, impl, p_block, seg_chunks, workspace)
+    _raise(lib.ssd_chunk_scan_gated_norm(ctypes.byref(a), _ptr(z), _ptr(norm_weight),
+                                         _act(norm_weight), int(group_size), float(eps),
+                                         _ptr(out), _stream(stream)),
+           "ssd_chunk_scan_gated_norm")
+    return out, final_states
+
+
+def _scan_args(lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus,
+               initial_states, has_initial_state, y, final_states, return_final_states, status,
+               impl, p_block, seg_chunks, workspace):
+    """ssd_scan_args for one scan call, with the outputs (and a workspace from torch's
+    allocator, when the plan wants one and none was passed) made where missing."""
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
     nseq = cu_seqlens.shape[0] - 1
@@ -211,8 +262,7 @@ def chunk_scan(x, dt, A, B, C, *, cu_seqlens, chunk_size, D=None, dt_bias=None,
     if workspace is not None:
         _check(workspace, "workspace", torch.uint8, None, dev)
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
-    _raise(lib.ssd_chunk_scan(ctypes.byref(a), _stream(stream)), "ssd_chunk_scan")
-    return y, final_states
+    return a, y, final_states, workspace
 
 
 def chunk_scan_workspace_size(x, B, C, *, cu_seqlens, chunk_size, impl="auto", p_block=0,

@@ -180,6 +180,19 @@ def decode_layer_step(pool, state_indices, x, dt, A, B, C, z, norm_weight, *, gr
     return pool, y, out, st
 
 
+def scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, group_size, eps=1e-5, D=None,
+                    dt_bias=None, dt_softplus=True, initial_states=None, has_initial_state=None,
+                    cu_seqlens=None):
+    """The prefill half of the layer in its order (scan with D skip, then the gated norm
+    of the scan's output).  Returns (y [T, H, P], final_states, out [T, H*P])."""
+    y, fs = scan_seq(x, dt, A, B, C, D=D, dt_bias=dt_bias, dt_softplus=dt_softplus,
+                     initial_states=initial_states, has_initial_state=has_initial_state,
+                     cu_seqlens=cu_seqlens)
+    T, H, P = y.shape
+    out = gated_rmsnorm(y.reshape(T, H * P), z, norm_weight, group_size=group_size, eps=eps)
+    return y, fs, out
+
+
 def state_copy(src_pool, src_idx, dst_pool, dst_idx):
     """Slot copy: for each pair with both indices >= 0, the destination slot becomes the
     source slot; a pair with an index outside [-1, slots) is skipped and raises the

@@ -22,8 +22,9 @@ def lib():
 def test_exports_every_declared_entry_point(lib):
     names = ssd.header_functions()
     assert set(names) == {"ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
-                          "ssd_chunk_scan_static_ws", "ssd_state_update",
-                          "ssd_state_update_multi", "ssd_decode_layer_step", "ssd_state_copy", "gated_rmsnorm", "ssd_read_status",
+                          "ssd_chunk_scan_static_ws", "ssd_chunk_scan_gated_norm",
+                          "ssd_state_update", "ssd_state_update_multi", "ssd_decode_layer_step",
+                          "ssd_state_copy", "gated_rmsnorm", "ssd_read_status",
                           "ssd_status_string", "ssd_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
                          check=True).stdout
@@ -76,6 +77,34 @@ def test_scan_rejects_bad_arguments(lib, bad):
     a = _scan_args(**bad)
     assert lib.ssd_chunk_scan(ctypes.byref(a), None) == 1
     assert lib.ssd_chunk_scan(None, None) == 1
+
+
+W = ctypes.c_void_p(0x9000)
+
+
+def _scan_norm(lib, a, z=0x20000, w=W, wt=None, gs=16, eps=1e-5, out=0x40000):
+    wt = ssd.SSD_F32 if wt is None else wt
+    return lib.ssd_chunk_scan_gated_norm(ctypes.byref(a), ctypes.c_void_p(z), w, wt, gs,
+                                         ctypes.c_float(eps), ctypes.c_void_p(out), None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(gs=0), dict(gs=7), dict(eps=-1.0), dict(eps=float("nan")), dict(w=None), dict(wt=5),
+    dict(out=0), dict(z=0x1000),                   # z overlaps y
+    dict(z=0x40000 + 4 * 8 * 64 - 4),              # z overlaps out by one element
+])
+def test_scan_gated_norm_rejects_bad_arguments(lib, bad):
+    """Checked before any launch: the norm's parameters, and a z sharing bytes with y or
+    out (the norm may read z while the scan is still writing)."""
+    a = _scan_args()
+    kw = dict(bad)
+    if kw.get("out") == 0:
+        a.y = None                                  # no y and no out: nothing to write to
+    assert _scan_norm(lib, a, **kw) == 1
+    assert lib.ssd_chunk_scan_gated_norm(None, None, W, ssd.SSD_F32, 16, ctypes.c_float(0.),
+                                         None, None) == 1
+    bad_scan = _scan_args(H=3)
+    assert _scan_norm(lib, bad_scan) == 1
 
 
 def test_scan_workspace_size(lib):

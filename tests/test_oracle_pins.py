@@ -426,3 +426,30 @@ def test_bf16_half_ulp_matches_rounding():
     assert np.all(np.abs(r - v) <= bf16_half_ulp(v))
     assert np.max(np.abs(r - v) / bf16_half_ulp(v)) > 0.99   # and it is tight
     assert bf16_half_ulp(16.3) == 2.0 ** -4
+
+
+@pytest.mark.parametrize("gs", [1536, 128, 64])
+def test_norm_carried_rounding_bounds_rounding_y(oracle_mod, gs):
+    """The allowance the scan + norm test gives for y stored in bf16 between the two ops
+    bounds what that rounding alone does to the norm's output (the oracle's norm of the
+    exact y against its norm of y rounded to bf16), and stays small: its median is a
+    small fraction of the 5e-2 max-abs bar."""
+    torch = pytest.importorskip("torch")
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from tolerance import norm_carried_rounding
+    rng = np.random.default_rng(97 + gs)
+    rows, d = 48, 1536
+    # heavy-tailed y (|y| up to about 40) and wide z, the hard case for the bound
+    y = rng.standard_normal((rows, d)) * 3.0 * np.exp(0.7 * rng.standard_normal((rows, d)))
+    bf = lambda a: torch.tensor(a.astype(np.float32)).to(torch.bfloat16).double().numpy()  # noqa
+    z = bf(1.5 * rng.standard_normal((rows, d)))
+    w = bf(1.0 + 0.1 * rng.standard_normal(d))
+    exact = oracle_mod.gated_rmsnorm(y, z, w, group_size=gs, eps=1e-5)
+    rounded = oracle_mod.gated_rmsnorm(bf(y), z, w, group_size=gs, eps=1e-5)
+    allow = norm_carried_rounding(y, z, w, gs, 1e-5)
+    diff = np.abs(exact - rounded)
+    assert np.all(diff <= allow)
+    assert np.max(diff / allow) > 0.3          # the bound is not loose by orders
+    assert np.median(allow) < 2e-3
+

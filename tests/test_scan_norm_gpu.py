@@ -1,0 +1,184 @@
+"""ssd_chunk_scan_gated_norm: the scan, then the gated RMSNorm over its output, in one
+call, with the norm launched as a programmatic dependent of the scan (its blocks load z
+while the scan runs and wait for it before reading y).
+
+Each case is held to the bar against the oracle's composition (scan, then gated norm)
+and, bit for bit, to ssd_chunk_scan followed by gated_rmsnorm as two plain calls.  The
+outputs start as NaN, so a norm that read y before the scan had written it would show.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mamba2_ssd_state_gb300 import inputs as I
+from mamba2_ssd_state_gb300 import ssd
+from gpu_util import dev
+from tolerance import TINY, check_bf16, check_fp32, norm_carried_rounding, rtol_K, scan_K
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev_inputs(s):
+    hi = None if s.has_initial_state is None else torch.from_numpy(s.has_initial_state).cuda()
+    return dict(x=dev(s.x), dt=dev(s.dt), A=dev(s.A), B=dev(s.B), C=dev(s.C), D=dev(s.D),
+                dt_bias=dev(s.dt_bias), initial_states=dev(s.initial_states),
+                has_initial_state=hi, cu_seqlens=torch.from_numpy(s.cu_seqlens).cuda())
+
+
+def _nan(shape, dtype):
+    return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
+
+
+def _fused(s, n, gs, *, want_y, seg_chunks=0, z=True, graph=False):
+    d = _dev_inputs(s)
+    T, H, P = d["x"].shape
+    zt, wt = (dev(n.z) if z else None), dev(n.weight)
+    y = _nan((T, H, P), d["x"].dtype) if want_y else None
+    out = _nan((T, H * P), d["x"].dtype)
+    fs = _nan((s.nseq, H, P, s.N), torch.float32)
+    status = ssd.new_status()
+
+    def call():
+        ssd.chunk_scan_gated_norm(d["x"], d["dt"], d["A"], d["B"], d["C"], zt, wt,
+                                  cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size,
+                                  group_size=gs, eps=n.eps, D=d["D"], dt_bias=d["dt_bias"],
+                                  initial_states=d["initial_states"],
+                                  has_initial_state=d["has_initial_state"], y=y, out=out,
+                                  final_states=fs, status=status, seg_chunks=seg_chunks)
+
+    if graph:
+        call()                       # warm-up outside capture (any workspace, module load)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream()
+        with torch.cuda.stream(s2):
+            with torch.cuda.graph(g, stream=s2):
+                call()
+        torch.cuda.synchronize()
+        for _ in range(2):           # every replay starts from NaN outputs
+            out.fill_(float("nan"))
+            fs.fill_(float("nan"))
+            if y is not None:
+                y.fill_(float("nan"))
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+    else:
+        call()
+    _, bits = ssd.read_status(status)
+    return out, y, fs, bits
+
+
+def _separate(s, n, gs, *, seg_chunks=0, z=True):
+    d = _dev_inputs(s)
+    y, fs = ssd.chunk_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=d["cu_seqlens"],
+                           chunk_size=s.chunk_size, D=d["D"], dt_bias=d["dt_bias"],
+                           initial_states=d["initial_states"],
+                           has_initial_state=d["has_initial_state"], seg_chunks=seg_chunks)
+    T, H, P = y.shape
+    out = ssd.gated_rmsnorm(y.view(T, H * P), dev(n.z) if z else None, dev(n.weight),
+                            group_size=gs, eps=n.eps)
+    torch.cuda.synchronize()
+    return out, y, fs
+
+
+def _oracle(s, n, gs, z=True):
+    return oracle.scan_gated_norm(s.x.values, s.dt.values, s.A.values, s.B.values, s.C.values,
+                                  n.z.values if z else None, n.weight.values, group_size=gs,
+                                  eps=n.eps, D=s.D.values, dt_bias=s.dt_bias.values,
+                                  initial_states=None if s.initial_states is None
+                                  else s.initial_states.values,
+                                  has_initial_state=s.has_initial_state,
+                                  cu_seqlens=s.cu_seqlens)
+
+
+CASES = {
+    # Mamba2-130M-shaped layer: 2 x 2048 tokens, one norm group over d_inner = 1536
+    "mamba2_130m": (lambda: I.scan_workload("mamba2_130m"), 1536, 0),
+    # ragged varlen with empty and one-token sequences, split into 2-chunk segments
+    # (scan kernel, fix-up kernel, then the norm), norm groups of two heads
+    "varlen_split": (lambda: I.make_scan_inputs([700, 129, 1, 0, 300, 1000, 257, 128, 385],
+                                                H=4, P=64, G=2, N=128, chunk_size=256,
+                                                act="bf16", seed=171, init="all"), 128, 2),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("want_y", [True, False])
+def test_scan_gated_norm_bf16(case, want_y):
+    make, gs, seg = CASES[case]
+    s = make()
+    n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=173)
+    out, y, fs, bits = _fused(s, n, gs, want_y=want_y, seg_chunks=seg)
+    assert bits == 0
+    out_sep, y_sep, fs_sep = _separate(s, n, gs, seg_chunks=seg)
+    assert torch.equal(out, out_sep), "differs from the two plain calls"
+    assert torch.equal(fs, fs_sep)
+    if want_y:
+        assert torch.equal(y, y_sep)
+    yr, fr, outr = _oracle(s, n, gs)
+    # y is held in bf16 between the scan and the norm (the layer's activation type), and
+    # the norm's gain carries that rounding to out: the max-abs bar counts the error
+    # beyond it and beyond out's own rounding
+    T = yr.shape[0]
+    carried = norm_carried_rounding(yr.reshape(T, -1), n.z.values, n.weight.values, gs, n.eps)
+    check_bf16(f"{case} out", out.float().cpu().numpy(), outr, stored_bf16=True,
+               carried=carried)
+    check_bf16(f"{case} final", fs.cpu().numpy(), fr)
+    if want_y:
+        check_bf16(f"{case} y", y.float().cpu().numpy(), yr)
+
+
+def test_scan_gated_norm_in_a_cuda_graph():
+    """Captured once and replayed twice from NaN outputs: the dependent launch survives
+    capture, and each replay matches the plain calls bit for bit."""
+    make, gs, seg = CASES["mamba2_130m"]
+    s = make()
+    n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=177)
+    out, y, fs, bits = _fused(s, n, gs, want_y=True, seg_chunks=seg, graph=True)
+    assert bits == 0
+    out_sep, y_sep, fs_sep = _separate(s, n, gs, seg_chunks=seg)
+    assert torch.equal(out, out_sep)
+    assert torch.equal(y, y_sep)
+    assert torch.equal(fs, fs_sep)
+
+
+def test_scan_gated_norm_fp32_no_gate():
+    """fp32 activations (the SIMT scan), no gate, bit for bit to the plain calls.  y is
+    held to rtol(K) against the oracle; out to the oracle's composition within rtol(K)
+    of y carried through the norm's gain, plus rtol(group_size) of the norm's own
+    arithmetic."""
+    s = I.scan_workload("tiny_fp32")
+    gs = s.H * s.P
+    n = I.make_norm_inputs(s.x.values.shape[0], gs, gs, act="f32", seed=179)
+    out, y, fs, bits = _fused(s, n, gs, want_y=True, z=False)
+    assert bits == 0
+    out_sep, _, _ = _separate(s, n, gs, z=False)
+    assert torch.equal(out, out_sep)
+    yr, fr, ya, fa = oracle.scan_seq(s.x.values, s.dt.values, s.A.values, s.B.values,
+                                     s.C.values, D=s.D.values, dt_bias=s.dt_bias.values,
+                                     cu_seqlens=s.cu_seqlens, with_abs=True)
+    Ky, Kf = scan_K(s.cu_seqlens, s.H, s.P, s.N, None)
+    check_fp32("fp32 y", y.cpu().numpy(), yr, ya, Ky)
+    check_fp32("fp32 final", fs.cpu().numpy(), fr, fa, Kf)
+    T = yr.shape[0]
+    outr = oracle.gated_rmsnorm(yr.reshape(T, gs), None, n.weight.values, group_size=gs,
+                                eps=n.eps)
+    dy = (rtol_K(Ky) * ya + TINY).reshape(T, gs)
+    bar = (norm_carried_rounding(yr.reshape(T, gs), None, n.weight.values, gs, n.eps, dy=dy)
+           + rtol_K(gs) * np.abs(outr) + TINY)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - outr)
+    frac = float(np.max(err / bar))
+    print(f"[bar] fp32 out: worst element used {100 * frac:.3f}% of its bar")
+    assert frac <= 1.0
+
+
+def test_scan_gated_norm_no_tokens():
+    """T = 0: nothing to normalise; the final states are the initial states."""
+    s = I.make_scan_inputs([0, 0], H=2, P=64, G=1, N=128, chunk_size=256, act="bf16",
+                           seed=181, init="all")
+    n = I.make_norm_inputs(0, s.H * s.P, s.P, act="bf16", seed=183)
+    out, _, fs, bits = _fused(s, n, s.P, want_y=False)
+    assert bits == 0 and out.numel() == 0
+    assert torch.equal(fs.cpu(), torch.from_numpy(s.initial_states.values).float())
