@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -554,6 +555,133 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
         "tokens_per_s": s.T / (us / 1e6), "avg_launch_us": us, "split_into_segments": split,
         "unsplit_us": us1, "achieved_gbs": sb / (us / 1e6) / 1e9,
         "frac_hbm": sb / (us / 1e6) / 1e9 / hbm_peak}
+    res.update(measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind))
+    return res
+
+
+def layer_bytes(T, H, P, G, N, nseq):
+    """Algorithmic bytes of the prefill layer path (scan, D skip, gated norm) in bf16: x, z
+    and out 2HP each, B and C 2GN each and dt 4H per token, plus the norm weight; y is an
+    intermediate and not counted."""
+    return T * (6 * H * P + 4 * G * N + 4 * H) + 2 * H * P
+
+
+def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
+    """The prefill layer path (ssd_chunk_scan_gated_norm: scan + D skip + gated RMSNorm in
+    8 groups of 1024) at Nemotron-H shapes: single sequences of 1K..64K tokens, and a mixed
+    batch of 64 packed prefills of 128..4096 tokens with the decode update of 256 pooled
+    slots on a second stream.  Inputs are drawn on the device with torch's seeded generator
+    in the layer's distributions (tens of GB of values: too slow to draw on the host)."""
+    H, P, G, N = 128, 64, 8, 128
+    d = H * P
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    l2 = L2Flush(torch, dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+
+    def bf(t):
+        return t.to(torch.bfloat16)
+
+    def params():
+        u = torch.rand(H, generator=gen, device=dev) * (0.1 - 1e-3) + 1e-3
+        A = -torch.exp(torch.rand(H, generator=gen, device=dev) * math.log(16.0))
+        return torch.log(torch.expm1(u)), A, torch.randn(H, generator=gen, device=dev)
+
+    def inputs(T):
+        return dict(x=bf(torch.randn((T, H, P), generator=gen, device=dev)),
+                    dt=torch.randn((T, H), generator=gen, device=dev),
+                    B=bf(torch.randn((T, G, N), generator=gen, device=dev) / math.sqrt(N)),
+                    C=bf(torch.randn((T, G, N), generator=gen, device=dev) / math.sqrt(N)),
+                    z=bf(torch.randn((T, d), generator=gen, device=dev)))
+
+    bias, A, Dp = params()
+    wn = bf(1 + 0.1 * torch.randn(d, generator=gen, device=dev))
+
+    def layer_call(i, cu, nseq, out, fs, ws, st=None):
+        ssd.chunk_scan_gated_norm(i["x"], i["dt"], A, i["B"], i["C"], i["z"], wn, cu_seqlens=cu,
+                                  chunk_size=128, group_size=1024, eps=1e-5, D=Dp,
+                                  dt_bias=bias, out=out, final_states=fs, workspace=ws,
+                                  stream=st)
+
+    def prepare(lens):
+        T = int(sum(lens))
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+        i = inputs(T)
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        fs = torch.empty((len(lens), H, P, N), dtype=torch.float32, device=dev)
+        nws = ssd.chunk_scan_workspace_size(i["x"], i["B"], i["C"], cu_seqlens=cu, chunk_size=128)
+        ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+        return T, cu, i, out, fs, ws, nws > 0
+
+    def timed_flushed(fn, n=iters):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(n):
+            l2.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return float(np.median(ts))
+
+    single = {}
+    for L in (1024, 4096, 16384, 65536):
+        T, cu, i, out, fs, ws, split = prepare([L])
+        us = timed_flushed(lambda: layer_call(i, cu, 1, out, fs, ws))
+        lb = layer_bytes(T, H, P, G, N, 1)
+        single[str(L)] = {"us": us, "tokens_per_s": T / (us / 1e6), "split_into_segments": split,
+                          "achieved_gbs": lb / (us / 1e6) / 1e9,
+                          "frac_hbm": lb / (us / 1e6) / 1e9 / hbm_peak}
+        del i, out, fs, ws
+    res["layer_nemotron_h_single_sequence"] = {
+        "workload": "one sequence of L tokens, H=128 P=64 G=8 N=128, chunk 128: scan + D skip + "
+                    "gated RMSNorm (8 groups of 1024) in one call, L2 flushed between calls",
+        "algorithmic_bytes": "x, z, out 2HP + B, C 2GN + dt 4H per token (y not counted)",
+        "peak_kind": f"{peak_kind} hbm copy", "by_L": single}
+
+    # mixed: 64 packed prefills + a 256-slot decode update on a second stream
+    lens = np.random.default_rng(4243).integers(128, 4097, size=64)
+    T, cu, i, out, fs, ws, split = prepare(lens)
+    S = 256
+    pool = torch.randn((S, H, P, N), generator=gen, device=dev)
+    idx = torch.randperm(S, generator=gen, device=dev).to(torch.int32)
+    ux = bf(torch.randn((S, H, P), generator=gen, device=dev))
+    udt = torch.randn((S, H), generator=gen, device=dev)
+    uB = bf(torch.randn((S, G, N), generator=gen, device=dev) / math.sqrt(N))
+    uC = bf(torch.randn((S, G, N), generator=gen, device=dev) / math.sqrt(N))
+    uy = torch.empty((S, H, P), dtype=torch.bfloat16, device=dev)
+    s_dec = torch.cuda.Stream(device=dev)
+
+    def decode(st):
+        ssd.state_update(pool, idx, ux, udt, A, uB, uC, D=Dp, dt_bias=bias, y=uy, stream=st)
+
+    def mixed():
+        s_dec.wait_stream(stream)
+        decode(s_dec)
+        layer_call(i, cu, len(lens), out, fs, ws, st=stream)
+        stream.wait_stream(s_dec)
+
+    us_mixed = timed_flushed(mixed)
+    us_prefill = timed_flushed(lambda: layer_call(i, cu, len(lens), out, fs, ws))
+    us_decode = timed_flushed(lambda: decode(stream))
+    lb = layer_bytes(T, H, P, G, N, len(lens))
+    ub = update_bytes(S, S, H, P, G, N)
+    res["layer_nemotron_h_mixed"] = {
+        "workload": f"64 packed prefills of 128..4096 tokens ({T} tokens), H=128 P=64 G=8 "
+                    "N=128: scan + D skip + gated RMSNorm in one call, and the decode update "
+                    "of 256 pooled slots (all active) on a second stream; L2 flushed between "
+                    "iterations",
+        "wall_us": us_mixed, "tokens_per_s": (T + S) / (us_mixed / 1e6),
+        "prefill_alone_us": us_prefill, "decode_alone_us": us_decode,
+        "split_into_segments": split,
+        "achieved_gbs": (lb + ub) / (us_mixed / 1e6) / 1e9,
+        "frac_hbm": (lb + ub) / (us_mixed / 1e6) / 1e9 / hbm_peak,
+        "peak_kind": f"{peak_kind} hbm copy"}
+    del i, out, fs, ws, pool, l2
     return res
 
 

@@ -60,7 +60,7 @@ typedef struct CUstream_st* ssd_stream_t; /* same type as cudaStream_t */
 typedef enum {
   SSD_OK = 0,
   SSD_ERR_INVALID_ARG = 1,    /* NULL required pointer, negative or inconsistent size */
-  SSD_ERR_UNSUPPORTED = 2,    /* a valid request this build has no kernel for */
+  SSD_ERR_UNSUPPORTED = 2,    /* a valid request the library has no kernel for */
   SSD_ERR_A_NOT_NEGATIVE = 3, /* ssd_read_status: device saw A[h] not < 0 */
   SSD_ERR_INDEX = 4,          /* ssd_read_status: device saw a slot index out of range */
   SSD_ERR_SEQ_META = 5,       /* ssd_read_status: device saw malformed cu_seqlens */

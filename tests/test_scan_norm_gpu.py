@@ -182,3 +182,66 @@ def test_scan_gated_norm_no_tokens():
     out, _, fs, bits = _fused(s, n, s.P, want_y=False)
     assert bits == 0 and out.numel() == 0
     assert torch.equal(fs.cpu(), torch.from_numpy(s.initial_states.values).float())
+
+
+def test_layer_mixed_nemotron_h_shapes_with_concurrent_decode():
+    """The mixed layer workload at reduced size, Nemotron-H head shapes (H=128, P=64, G=8,
+    norm groups of 16 heads): six ragged packed prefills through the scan + norm call
+    while the decode update of 16 pooled slots runs on a second stream.  Both results
+    equal the same calls made one after the other, bit for bit; two norm groups and the
+    pool are held to the oracle."""
+    from gpu_util import scan_oracle
+    s = I.make_scan_inputs([300, 129, 1000, 1, 700, 257], H=128, P=64, G=8, N=128,
+                           chunk_size=128, act="bf16", seed=191, init=[1, 0, 1, 0, 0, 1])
+    T, gs = s.T, 1024
+    n = I.make_norm_inputs(T, 128 * 64, gs, act="bf16", seed=193)
+    S = 16
+    idx = np.random.default_rng(195).permutation(S).astype(np.int32)  # every slot active
+    u = I.make_update_inputs(S, idx, 128, 64, 8, 128, act="bf16", seed=197)
+    d = _dev_inputs(s)
+    zt, wt = dev(n.z), dev(n.weight)
+    didx = torch.from_numpy(idx).cuda()
+
+    def run(concurrent):
+        pool = dev(u.pool)
+        out = _nan((T, 128 * 64), torch.bfloat16)
+        fs = _nan((s.nseq, 128, 64, 128), torch.float32)
+        uy = _nan((S, 128, 64), torch.bfloat16)
+        status = ssd.new_status()
+        main = torch.cuda.current_stream()
+        side = torch.cuda.Stream() if concurrent else main
+        side.wait_stream(main)
+        ssd.state_update(pool, didx, dev(u.x), dev(u.dt), dev(u.A), dev(u.B), dev(u.C),
+                         D=dev(u.D), dt_bias=dev(u.dt_bias), y=uy, status=status, stream=side)
+        ssd.chunk_scan_gated_norm(d["x"], d["dt"], d["A"], d["B"], d["C"], zt, wt,
+                                  cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size,
+                                  group_size=gs, eps=n.eps, D=d["D"], dt_bias=d["dt_bias"],
+                                  initial_states=d["initial_states"],
+                                  has_initial_state=d["has_initial_state"], out=out,
+                                  final_states=fs, status=status, stream=main)
+        main.wait_stream(side)
+        _, bits = ssd.read_status(status)
+        assert bits == 0
+        return out, fs, pool, uy
+
+    out, fs, pool, uy = run(True)
+    out2, fs2, pool2, uy2 = run(False)
+    assert torch.equal(out, out2) and torch.equal(fs, fs2)
+    assert torch.equal(pool, pool2) and torch.equal(uy, uy2)
+    for grp in (0, 5):                                   # heads 16 grp .. 16 grp + 15
+        heads = list(range(16 * grp, 16 * grp + 16))
+        yr, fr = scan_oracle(s, heads=heads)
+        cols = slice(gs * grp, gs * (grp + 1))
+        outr = oracle.gated_rmsnorm(yr.reshape(T, gs), n.z.values[:, cols],
+                                    n.weight.values[cols], group_size=gs, eps=n.eps)
+        carried = norm_carried_rounding(yr.reshape(T, gs), n.z.values[:, cols],
+                                        n.weight.values[cols], gs, n.eps)
+        check_bf16(f"mixed group {grp} out", out[:, cols].float().cpu().numpy(), outr,
+                   stored_bf16=True, carried=carried)
+        check_bf16(f"mixed group {grp} final", fs[:, heads].cpu().numpy(), fr)
+    ref_pool, yr_dec, st = oracle.state_update(u.pool.values, idx, u.x.values, u.dt.values,
+                                               u.A.values, u.B.values, u.C.values,
+                                               D=u.D.values, dt_bias=u.dt_bias.values)
+    assert st == 0
+    check_bf16("mixed decode y", uy.float().cpu().numpy(), yr_dec)
+    check_bf16("mixed decode pool", pool.cpu().numpy(), ref_pool)
