@@ -179,31 +179,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int p0 = pbk * PB;
   const int H = prm.H, P = prm.P;
   const int g = h / (H / prm.G);
+  const float Ah = prm.A[h];  // issued first: nothing below depends on it until the test
 
-  int s = j, kseg = 0, nseg_s = 1;
+  int s = j, kseg = 0, nseg_s = 1, t0, t1;
   if constexpr (kSplit) {  // a separate instance: the plain chain carries none of this
-    __shared__ int seg_info[3];
-    if (threadIdx.x == 0) {
-      int ss = -1, kk = 0, nn = 0;
-      find_segment(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn);
-      seg_info[0] = ss;
-      seg_info[1] = kk;
-      seg_info[2] = nn;
+    __shared__ int seg_info[5];
+    if (warp == 0) {
+      int ss = -1, kk = 0, nn = 0, a = 0, b = 0;
+      find_segment_warp(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn, a, b);
+      if (lane == 0) {
+        seg_info[0] = ss;
+        seg_info[1] = kk;
+        seg_info[2] = nn;
+        seg_info[3] = a;
+        seg_info[4] = b;
+      }
     }
     __syncthreads();
     s = seg_info[0];
     kseg = seg_info[1];
     nseg_s = seg_info[2];
+    t0 = seg_info[3];
+    t1 = seg_info[4];
     if (s < 0) return;  // past the batch's last segment
+  } else {
+    t0 = prm.cu[s];
+    t1 = prm.cu[s + 1];
   }
   if (unit == 0 && threadIdx.x == 0 && (prm.cu[0] != 0 || prm.cu[prm.nseq] != prm.T))
     set_status(prm.status, SSD_DEV_SEQ_META);
-  const int t0 = prm.cu[s], t1 = prm.cu[s + 1];
   if (!(0 <= t0 && t0 <= t1 && t1 <= prm.T)) {
     if (threadIdx.x == 0) set_status(prm.status, SSD_DEV_SEQ_META);
     return;
   }
-  const float Ah = prm.A[h];
   const size_t PN = (size_t)P * NSTATE;
   // this CTA's chunks: [c0, c0 + nch) of the sequence, first token tb
   const int nch_s = (t1 - t0 + QT - 1) / QT;
@@ -292,16 +300,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // thread 0 is the TMA producer: chunk 0's tiles are on their way while the rest of
+    // the CTA sets up (the barriers they complete are the ones just initialised here)
+    for (int c = 1; c < 4 && c < nch; ++c) {  // L2 prefetch of the next chunks
+      tma_prefetch_3d(&tmB, 0, g, tb + c * QT);
+      tma_prefetch_3d(&tmB, 64, g, tb + c * QT);
+      tma_prefetch_3d(&tmC, 0, g, tb + c * QT);
+      tma_prefetch_3d(&tmC, 64, g, tb + c * QT);
+      tma_prefetch_3d(&tmX, p0, h, tb + c * QT);
+    }
+    if (nch > 0) {
+      mbar_arrive_expect_tx(&b_full[0], 32768);
+      tma_load_3d(sm + L::kB, &tmB, &b_full[0], 0, g, tb);
+      tma_load_3d(sm + L::kB + 16384, &tmB, &b_full[0], 64, g, tb);
+      mbar_arrive_expect_tx(&c_full[0], 32768);
+      tma_load_3d(sm + L::kC, &tmC, &c_full[0], 0, g, tb);
+      tma_load_3d(sm + L::kC + 16384, &tmC, &c_full[0], 64, g, tb);
+      mbar_arrive_expect_tx(&x_full[0], L::kXBytes);
+      tma_load_3d(sm + L::kX, &tmX, &x_full[0], p0, h, tb);
+    }
+  }
+  // the decay warp's first dt values, loaded during the set-up (strided by H: one sector
+  // per token, a full memory round trip)
+  float dt_first[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp == kDecayWarp && nch > 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int tok = tb + 32 * k + lane;
+      if (tok < t1) dt_first[k] = prm.dt[(size_t)tok * H + h];
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
     tc_fence_before();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmX);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmC);
   }
   __syncthreads();
   tc_fence_after();
@@ -326,11 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_3d(&tmC, 64, g, tok);
         tma_prefetch_3d(&tmX, p0, h, tok);
       };
-      for (int c = 0; c < kAhead && c < nch; ++c) prefetch(c);
-      int nb_iss = 0, nc_iss = 0, nx_iss = 0;
+      // chunk 0's tiles and the prefetch of chunks 1..3 were issued during the set-up
+      int nb_iss = nch > 0, nc_iss = nch > 0, nx_iss = nch > 0;
       for (int c = 0; c < nch; ++c) {
         const int tok = tb + c * QT;
         if (c + kAhead < nch) prefetch(c + kAhead);
+        if (c == 0) continue;
         const int sb = c % NBB, sc = c % NBC, sx = c % NX;
         if (c >= NBB && !mbar_wait(&b_empty[sb], ((c / NBB) - 1) & 1, abort_flag, kWaitLimit))
           break;
@@ -373,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         dt_raw[k] = tok < t1 ? prm.dt[(size_t)tok * H + h] : 0.f;
       }
     };
-    if (nch > 0) load_dt(0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dt_raw[k] = dt_first[k];
     // split sequences: each token's log2 decay from its segment start, for the fix-up
     float* cs_out = (kSplit && split && pbk == 0) ? prm.ws_cs + h : nullptr;
     float seg_off = 0.f;
@@ -853,21 +887,25 @@ __global__ void __launch_bounds__(kFixThreads, 1)
   const int j = unit / (prm.npb * prm.H);
   const int p0 = pbk * PB;
   const int H = prm.H, P = prm.P;
-  __shared__ int seg_info[3];
+  __shared__ int seg_info[5];
   const int tr_unit = 2 * prm.H * prm.npb;  // the CTA a trace build records
   (void)tr_unit;
   if (threadIdx.x == 0) TRACE_FIX(0, 0, tr_unit);
-  if (threadIdx.x == 0) {
-    int ss = -1, kk = 0, nn = 0;
-    find_segment(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn);
-    seg_info[0] = ss;
-    seg_info[1] = kk;
-    seg_info[2] = nn;
+  if (threadIdx.x < 32) {
+    int ss = -1, kk = 0, nn = 0, a = 0, b = 0;
+    find_segment_warp(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn, a, b);
+    if (threadIdx.x == 0) {
+      seg_info[0] = ss;
+      seg_info[1] = kk;
+      seg_info[2] = nn;
+      seg_info[3] = a;
+      seg_info[4] = b;
+    }
   }
   __syncthreads();
   const int s = seg_info[0], kseg = seg_info[1], nseg_s = seg_info[2];
   if (s < 0 || kseg == 0) return;  // a first segment has nothing to add
-  const int t0 = prm.cu[s], t1 = prm.cu[s + 1];
+  const int t0 = seg_info[3], t1 = seg_info[4];
   if (!(0 <= t0 && t0 <= t1 && t1 <= prm.T)) return;  // reported by the scan kernel
   const float Ah = prm.A[h];
   if (!(Ah < 0.f)) return;  // the scan kernel zeroed that head
@@ -1209,8 +1247,10 @@ int min_segc(const ssd_scan_args& a) {
 // mask and C.B^T work does not shrink with PB; kRamp is the pipeline fill of its first
 // chunk).  A split adds the fix-up grid over the later segments, one CTA per SM: a
 // fixed cost per wave (its launch, set-up and first tile), one chained step per segment
-// before it (the entering state) and about 0.4 of a scan chunk per chunk.
-constexpr double kRamp = 3.0, kFixBase = 7.0, kFixPerSeg = 0.4, kFixPerChunk = 0.4;
+// before it (the entering state) and about 0.4 of a scan chunk per chunk.  (kFixBase
+// also carries what a split costs the scan grid itself beyond its chunks; it fell from 7
+// to 5 once both kernels found their segment in one warp-wide pass over the lengths.)
+constexpr double kRamp = 3.0, kFixBase = 5.0, kFixPerSeg = 0.4, kFixPerChunk = 0.4;
 
 double plan_cost(const ssd_scan_args& a, int pb, int segc) {
   const int sms = sm_count();

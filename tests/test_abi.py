@@ -122,8 +122,12 @@ def test_scan_workspace_size(lib):
     assert size(seg_chunks=-1) == 0                       # never split
     assert size(seg_chunks=4, impl=1) == 0                # SIMT path: no workspace
     assert size(seg_chunks=4, act_dtype=ssd.SSD_F32) == 0  # not a tensor-core shape
-    # the planner keeps two 2048-token sequences whole, and splits one of 16384 tokens
-    assert size() == 0
+    # the planner cuts two 2048-token sequences into 6-chunk segments (channel block 64:
+    # 2 x 3 x 24 = 144 CTAs, one wave), keeps a Nemotron-H-shaped batch whole, and
+    # splits one sequence of 16384 tokens
+    assert size() == r256((2 + (4096 + 127 * 2) // (128 * 6)) * 24 * 64 * 128 * 4
+                          + 4096 * 24 * 4)
+    assert size(nseq=4, T=16384, H=128, G=8) == 0
     auto = size(nseq=1, T=16384)
     assert auto > 0 and auto % 256 == 0
     assert lib.ssd_chunk_scan_workspace_size(None) == 0
