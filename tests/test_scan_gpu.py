@@ -275,6 +275,26 @@ def test_many_short_sequences_tc():
     np.testing.assert_array_equal(fs[empty], s.initial_states.values[empty])
 
 
+@pytest.mark.parametrize("seg", [1, 2])
+def test_split_many_sequences_segment_lookup(seg):
+    """70 packed sequences (empty, one token, up to five chunks) split into segments of
+    1 or 2 chunks: each CTA of the scan and of the fix-up finds its segment with one
+    warp reading the lengths 32 sequences at a time, so the lookup crosses three groups
+    of 32, with segment counts that differ from sequence to sequence."""
+    rng = np.random.default_rng(509)
+    lens = rng.choice([0, 1, 127, 128, 129, 300, 600], size=70)
+    init = (rng.random(70) < 0.5).astype(int).tolist()
+    s = I.make_scan_inputs(lens.tolist(), H=2, P=64, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=511, init=init)
+    y, fs, bits = scan_gpu(s, impl="tc", seg_chunks=seg)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16(f"70 seqs seg {seg} y", y, yr)
+    check_bf16(f"70 seqs seg {seg} final", fs, fr)
+    empty = np.flatnonzero(lens == 0)
+    np.testing.assert_array_equal(fs[empty], s.initial_states.values[empty])
+
+
 def test_tc_headdim_128_group_per_head():
     """P = 128 (two 64-channel blocks per head), G = H: every head its own B and C."""
     s = I.make_scan_inputs([300, 77, 513], H=3, P=128, G=3, N=128, chunk_size=128, act="bf16",
