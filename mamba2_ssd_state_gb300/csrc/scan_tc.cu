@@ -609,7 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(e2[e]);
-            e2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+            float a, b;
+            mul_f32x2(a, b, f.x, f.y, w, w);
+            e2[e] = __floats2bfloat162_rn(a, b);
           }
           *reinterpret_cast<uint4*>(sm + L::kXs + (c % NXS) * L::kXPad + off) = xv;
         }
@@ -648,10 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 f = cf[e4];
-            m[4 * e4 + 0] *= rowf * f.x;
-            m[4 * e4 + 1] *= rowf * f.y;
-            m[4 * e4 + 2] *= rowf * f.z;
-            m[4 * e4 + 3] *= rowf * f.w;
+            float t0, t1, t2, t3;  // rowf * colf, then times C.B^T, two lanes at a time
+            mul_f32x2(t0, t1, rowf, rowf, f.x, f.y);
+            mul_f32x2(t2, t3, rowf, rowf, f.z, f.w);
+            mul_f32x2(m[4 * e4 + 0], m[4 * e4 + 1], m[4 * e4 + 0], m[4 * e4 + 1], t0, t1);
+            mul_f32x2(m[4 * e4 + 2], m[4 * e4 + 3], m[4 * e4 + 2], m[4 * e4 + 3], t2, t3);
           }
         } else {
 #pragma unroll
@@ -729,7 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sv[16];
         tmem_ld16(tmem + lrow + L::kS + (c % NXS) * PB + 16 * sl, sv);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) hreg[16 * sl + e] = fmaf(e_l, hreg[16 * sl + e], sv[e]);
+        for (int e = 0; e < 16; e += 2)
+          fma_f32x2(hreg[16 * sl + e], hreg[16 * sl + e + 1], e_l, e_l, hreg[16 * sl + e],
+                    hreg[16 * sl + e + 1], sv[e], sv[e + 1]);
       }
       tc_fence_before();
       __syncwarp();
@@ -759,10 +764,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 o[2];
         uint32_t* o32 = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 8; ++e) {  // y = D x + (2^cs_i Yoff + Y), two channels at a time
           const float2 xf = __bfloat1622float2(x2[e]);
-          o32[e] = pack_bf16(fmaf(e_i, yo[2 * e], yv[2 * e]) + Dh * xf.x,
-                             fmaf(e_i, yo[2 * e + 1], yv[2 * e + 1]) + Dh * xf.y);
+          float a, b;
+          fma_f32x2(a, b, e_i, e_i, yo[2 * e], yo[2 * e + 1], yv[2 * e], yv[2 * e + 1]);
+          fma_f32x2(a, b, Dh, Dh, xf.x, xf.y, a, b);
+          o32[e] = pack_bf16(a, b);
         }
         if (tok < t1) {
           reinterpret_cast<uint4*>(yrow + 16 * sl)[0] = o[0];
