@@ -112,6 +112,11 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  *   chunk_size: 1 .. 256 (the tensor-core path takes 64, 128 or 256)
  *   impl: SSD_IMPL_*; p_block: 0 = choose, else the channel split of the tensor-core
  *     path (16, 32 or 64; must divide P)
+ *   head_block: heads per CTA of the tensor-core path: 0 = choose, 1 = one head, 2 = two
+ *     heads of one group sharing the C.B^T product and the B and C tiles (needs H and
+ *     H/G even, P % 64 == 0 and p_block 0 or 64; like p_block it shapes only the
+ *     tensor-core path: impl = SSD_IMPL_TC on a shape it cannot take returns
+ *     SSD_ERR_UNSUPPORTED, SSD_IMPL_AUTO then runs the SIMT path)
  *   seg_chunks, workspace, workspace_bytes: sequence splitting of the tensor-core path
  *     (see ssd_chunk_scan_workspace_size; zeros = run unsplit; -1 <= seg_chunks, and a
  *     nonzero workspace_bytes needs a workspace pointer, else SSD_ERR_INVALID_ARG)
@@ -145,6 +150,7 @@ typedef struct {
   int32_t seg_chunks;
   void* workspace;
   size_t workspace_bytes;
+  int32_t head_block;
 } ssd_scan_args;
 
 SSD_API ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream);
@@ -179,9 +185,10 @@ SSD_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args);
  * Same arguments, results and errors as ssd_chunk_scan, except that the workspace is a
  * 16 MiB device array owned by the library (part of its image, one per device):
  *   - args->workspace must be NULL and workspace_bytes 0 (else SSD_ERR_INVALID_ARG);
- *   - a call whose plan wants more than 16 MiB (ssd_chunk_scan_workspace_size) returns
- *     SSD_ERR_UNSUPPORTED before launching anything: pass seg_chunks = -1 (no split) or
- *     use ssd_chunk_scan with a workspace of the caller's;
+ *   - with seg_chunks = 0 the plan is the best one whose workspace fits in 16 MiB
+ *     (unsplit if none does); an explicit seg_chunks >= 1 whose workspace exceeds 16 MiB
+ *     returns SSD_ERR_UNSUPPORTED before launching anything (use ssd_chunk_scan with a
+ *     workspace of the caller's instead);
  *   - nothing in the array needs clearing between calls;
  *   - the array is shared by every call on a device: calls that can overlap in time (on
  *     different streams, or from different threads) race on it and must be ordered by

@@ -99,14 +99,6 @@ constexpr uint32_t kColAcc = 192; // Y[2], S, Yoff[2]: PB columns each (5 PB <= 
 constexpr int kProCs = 0, kProDt = QT, kProColf = 2 * QT, kProW = 3 * QT, kProSafe = 4 * QT;
 constexpr int kProStride = 4 * QT + 8;  // floats
 
-#ifdef SSD_TRACE
-__device__ long long g_trace[64][16];
-#define TRACE(c, slot) \
-  do { if (blockIdx.x == 0 && (c) < 64) g_trace[(c)][(slot)] = clock64(); } while (0)
-#else
-#define TRACE(c, slot) do { } while (0)
-#endif
-
 struct TcParams {
   const float* dt;
   const float* dt_bias;
@@ -384,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&x_full[sx], L::kXBytes);
         tma_load_3d(sm + L::kX + sx * L::kXPad, &tmX, &x_full[sx], p0, h, tok);
         nx_iss = c + 1;
-        TRACE(c, 0);
       }
       // every copy issued must have landed before the CTA's shared memory is released
       for (int c = nb_iss > NBB ? nb_iss - NBB : 0; c < nb_iss; ++c)
@@ -414,7 +405,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB;
       if (c >= NB && !wwait(&pro_empty[b], ((c / NB) - 1) & 1)) break;
-      TRACE(c, 1);
       // dt, base-2 decay a = dt A log2(e), inclusive cumulative sum over the 128 tokens
       float d[4], cs[4], carry = 0.f;
 #pragma unroll
@@ -473,7 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #else
       if (lane == 0) mbar_arrive(&pro_full[b]);
 #endif
-      TRACE(c, 2);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0)
@@ -517,7 +506,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    dXs + (uint64_t)((ns % NXS) * (L::kXPad >> 4)) + kk * L::kXRow, idS, kk > 0);
           mma_commit(&s_full[ns % NXS]);
           mma_commit(&b_empty[ns % NBB]);
-          TRACE(ns, 9);
           ++ns;
           progress = true;
         }
@@ -525,7 +513,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nyo < ncb && mbar_test_wait(&h_ready[(nyo + 1) & 1], (nyo >> 1) & 1) &&
             (nyo < 2 || mbar_test_wait(&y_empty[nyo & 1], ((nyo >> 1) - 1) & 1))) {
           tc_fence_after();
-          TRACE(nyo, 4);
           const uint64_t da = dC_k0 + (uint64_t)((nyo % NBC) * (32768 >> 4));
           const uint64_t db = dHT0 + (uint64_t)(((nyo + 1) & 1) * (L::kHTPad >> 4));  // h_{k-1}
 #pragma unroll
@@ -547,14 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 8; ++kk)  // K = N = 128 in steps of 16 (32 bytes)
             mma_ss(tmem + kColCB, da + kstep_k(kk), db + kstep_k(kk), idCB, kk > 0);
           mma_commit(cb_full);
-          TRACE(ncb, 10);
           ++ncb;
           progress = true;
         }
         if (ny < ncb && mbar_test_wait(m_ready, ny & 1) &&
             (ny < 2 || mbar_test_wait(&y_empty[ny & 1], ((ny >> 1) - 1) & 1))) {
           tc_fence_after();
-          TRACE(ny, 3);
           const uint64_t db = dX0 + (uint64_t)((ny % NX) * (L::kXPad >> 4));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // Y = M x : K = 128 tokens, M from TMEM (8 cols/step)
@@ -597,7 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       //     previous chunk's S product is done
       // this chunk's w o x tile was last read by S(c - NXS)
       if (c >= NXS && !wwait(&s_full[c % NXS], ((c / NXS) - 1) & 1)) break;
-      if (warp == 2) TRACE(c, 5);
       {
         const float w = pb[kProW + r];
         const uint8_t* xt = sm + L::kX + sx * L::kXPad;
@@ -619,7 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&xs_ready[c % NXS]);
-      if (warp == 2) TRACE(c, 14);
       // (2) the decay mask from C.B^T
       if (!wwait(cb_full, c & 1)) break;
       tc_fence_after();
@@ -671,7 +654,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[jj][e] = pack_bf16(m[2 * e], m[2 * e + 1]);
       }
-      if (warp == 2) TRACE(c, 12);
       // M of the previous chunk is free once its Y product is done
       if (c >= 1 && !wwait(&y_full[(c - 1) & 1], ((c - 1) >> 1) & 1)) break;
       tc_fence_after();
@@ -686,7 +668,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&x_empty[sx]);
         mbar_arrive(&pro_empty[b]);
       }
-      if (warp == 2) TRACE(c, 6);
     }
   } else {
     // ------------------------------------------------------------ output warps
@@ -723,7 +704,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wwait(&pro_full[b], (c / NB) & 1))) break;
       if (!(ok = wwait(&s_full[c % NXS], (c / NXS) & 1))) break;
       tc_fence_after();
-      if (warp == 2 + kMaskWarps) TRACE(c, 7);
       const float* pb = pro + b * kProStride;
       // state first: h = 2^cs_last h + S, then h^T for the next chunk's Yoff
       const float e_l = ex2(pb[kProCs + QT - 1]);
@@ -740,13 +720,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[c % NXS]);
       if (c + 1 < nch) write_hT(c & 1);
-      if (warp == 2 + kMaskWarps) TRACE(c, 11);
       // then y = Y + 2^cs_i Yoff + D x
       if (!(ok = wwait(&y_full[c & 1], (c >> 1) & 1))) break;
       if (!(ok = wwait(&yoff_full[c & 1], (c >> 1) & 1))) break;
       if (!(ok = wwait(&x_full[sx], (c / NX) & 1))) break;
       tc_fence_after();
-      if (warp == 2 + kMaskWarps) TRACE(c, 13);
       const float e_i = ex2(pb[kProCs + r]);
       const int tok = tb + c * QT + r;
       __nv_bfloat16* yrow = prm.y + ((size_t)tok * H + h) * P + p0;
@@ -783,7 +761,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&x_empty[sx]);
         mbar_arrive(&pro_empty[b]);
       }
-      if (warp == 2 + kMaskWarps) TRACE(c, 8);
     }
     // the final state, or a segment's local end state (the fix-up kernel chains those)
     float* hout = ok ? end_state() : nullptr;
@@ -801,15 +778,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) set_status(prm.status, SSD_DEV_TIMEOUT);
 }
 
-#ifdef SSD_TRACE
-}  // namespace
-extern "C" SSD_API int ssd_trace_read(long long* dst) {
-  return (int)cudaMemcpyFromSymbol(dst, g_trace, sizeof(g_trace));
-}
-namespace {
-#endif
-
-
 #ifdef SSD_FAULT_INJECT
 }  // namespace
 extern "C" SSD_API int ssd_test_withhold_chunk(int chunk) {
@@ -817,6 +785,14 @@ extern "C" SSD_API int ssd_test_withhold_chunk(int chunk) {
 }
 namespace {
 #endif
+}  // namespace
+}  // namespace ssd
+
+#include "scan_pair.cuh"
+
+namespace ssd {
+namespace {
+
 // ------------------------------------------------------------------ split sequences
 //
 // When a sequence is split into segments, segment k > 0 was scanned from a zero state and
@@ -832,21 +808,6 @@ namespace {
 // final state.  It is launched with programmatic stream
 // serialisation: its set-up and its C loads overlap the scan kernel's tail, and it waits
 // for the scan to complete before it reads what the scan wrote.
-
-#ifdef SSD_TRACE
-__device__ long long g_trace_fix[32][4];
-#define TRACE_FIX(i, slot, unit_id)                                                   \
-  do {                                                                                \
-    if (blockIdx.x == (unit_id) && (i) < 32) g_trace_fix[(i)][(slot)] = clock64();    \
-  } while (0)
-}  // namespace
-extern "C" SSD_API int ssd_trace_fix_read(long long* dst) {
-  return (int)cudaMemcpyFromSymbol(dst, g_trace_fix, sizeof(g_trace_fix));
-}
-namespace {
-#else
-#define TRACE_FIX(i, slot, unit_id) do { } while (0)
-#endif
 
 constexpr int kMaxSegs = 64;      // segments per sequence (the planner keeps to it)
 constexpr int kFixThreads = 192;  // warp 0 TMA, warp 1 TMEM + MMA, warps 2-5 epilogue
@@ -895,9 +856,6 @@ __global__ void __launch_bounds__(kFixThreads, 1)
   const int p0 = pbk * PB;
   const int H = prm.H, P = prm.P;
   __shared__ int seg_info[5];
-  const int tr_unit = 2 * prm.H * prm.npb;  // the CTA a trace build records
-  (void)tr_unit;
-  if (threadIdx.x == 0) TRACE_FIX(0, 0, tr_unit);
   if (threadIdx.x < 32) {
     int ss = -1, kk = 0, nn = 0, a = 0, b = 0;
     find_segment_warp(prm.cu, prm.nseq, prm.segc, j, ss, kk, nn, a, b);
@@ -910,14 +868,24 @@ __global__ void __launch_bounds__(kFixThreads, 1)
     }
   }
   __syncthreads();
+  // A CTA with nothing to do still waits for the scan grid before it leaves, so that this
+  // grid never completes before the scan does: a programmatic dependent of this kernel
+  // (the norm of the scan + norm call) relies on that to read the scan's outputs.
   const int s = seg_info[0], kseg = seg_info[1], nseg_s = seg_info[2];
-  if (s < 0 || kseg == 0) return;  // a first segment has nothing to add
+  if (s < 0 || kseg == 0) {  // a first segment has nothing to add
+    griddep_wait();
+    return;
+  }
   const int t0 = seg_info[3], t1 = seg_info[4];
-  if (!(0 <= t0 && t0 <= t1 && t1 <= prm.T)) return;  // reported by the scan kernel
   const float Ah = prm.A[h];
-  if (!(Ah < 0.f)) return;  // the scan kernel zeroed that head
+  // malformed lengths are reported by the scan kernel; it zeroed heads with A not < 0
+  if (!(0 <= t0 && t0 <= t1 && t1 <= prm.T) || !(Ah < 0.f)) {
+    griddep_wait();
+    return;
+  }
   if (nseg_s > kMaxSegs) {  // the planner never gets here; a malformed batch might
     if (threadIdx.x == 0) set_status(prm.status, SSD_DEV_SEQ_META);
+    griddep_wait();
     return;
   }
   const int seg_tokens = prm.segc * QT;
@@ -1035,7 +1003,6 @@ __global__ void __launch_bounds__(kFixThreads, 1)
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
     // everything below reads what the scan kernel wrote
     griddep_wait();
-    if (r == 0) TRACE_FIX(0, 2, tr_unit);
     // d_i: the decay from segment i's start to its last token, as the scan kernel left it
     auto seg_decay = [&](int i) -> float {
       const int te = min(t1, t0 + (i + 1) * seg_tokens);
@@ -1067,7 +1034,6 @@ __global__ void __launch_bounds__(kFixThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(h_ready);
     }
-    if (r == 0) TRACE_FIX(0, 3, tr_unit);
     if (last && prm.fin) {  // final state = 2^{d_last} H_last + L_last
       const float d = ex2(seg_decay(kseg));
       const float* ll = loc0 + (size_t)kseg * H * PN;
@@ -1096,13 +1062,11 @@ __global__ void __launch_bounds__(kFixThreads, 1)
       const bool full_tile = tb + (c + 1) * QT <= t1;
       const float scale = ex2(csn);
       if (c + 1 < nch) load_cs(c + 1);
-      if (r == 0) TRACE_FIX(1 + c, 0, tr_unit);
       const int sy = c % NY;
       // A wait that fails (an abort) skips this chunk's work, but every epilogue warp still
       // reaches the named barrier below, which ORs the failures, so they all leave the
       // loop there together: a warp leaving early would strand the others in the barrier.
       const bool ok = wwait(&acc_full[st], (c >> 1) & 1) && wwait(&y_full[sy], (c / NY) & 1);
-      if (r == 0) TRACE_FIX(1 + c, 1, tr_unit);
       tc_fence_after();
       uint8_t* yt = sm + L::kY + sy * L::kYPad;
 #pragma unroll
@@ -1146,7 +1110,6 @@ __global__ void __launch_bounds__(kFixThreads, 1)
           bulk_wait_read_one();
           mbar_arrive(&y_free[(c - 1) % NY]);
         }
-        TRACE_FIX(1 + c, 2, tr_unit);
       }
       done_c = c + 1;
     }
@@ -1213,9 +1176,11 @@ int sm_count() {
   return n;
 }
 
-// How one call runs: channel block PB, segment length segc (0 = sequences are not split),
-// the segment count the grid covers and the workspace that needs.
+// How one call runs: heads per CTA hb (1, or 2 for the pair kernel), channel block PB,
+// segment length segc (0 = sequences are not split), the segment count the grid covers
+// and the workspace that needs.
 struct ScanPlan {
+  int hb = 1;
   int pb = 0;
   int segc = 0;
   long long nseg = 0;
@@ -1246,61 +1211,83 @@ int min_segc(const ssd_scan_args& a) {
   return (int)std::max<long long>(1, (nch_max + kMaxSegs - 1) / kMaxSegs);
 }
 
-// Cost model in units of one 128-token chunk of a 64-channel CTA in its steady state
-// (about 2 us), fitted to measured times of the 2 x 2048-token and 4-sequence varlen
-// batches and of single 16K-token sequences.  The host sees only T and nseq (the
-// lengths live on the device), so sequences are taken as equally long.  One CTA per SM;
-// a CTA of channel block PB that runs n chunks costs about kRamp + n (1 + PB/256) (the
-// mask and C.B^T work does not shrink with PB; kRamp is the pipeline fill of its first
-// chunk).  A split adds the fix-up grid over the later segments, one CTA per SM: a
-// fixed cost per wave (its launch, set-up and first tile), one chained step per segment
-// before it (the entering state) and about 0.4 of a scan chunk per chunk.  (kFixBase
-// also carries what a split costs the scan grid itself beyond its chunks; it fell from 7
-// to 5 once both kernels found their segment in one warp-wide pass over the lengths.)
-constexpr double kRamp = 3.0, kFixBase = 5.0, kFixPerSeg = 0.4, kFixPerChunk = 0.4;
+// The pair kernel takes two heads of one group per CTA, 64 channels each.
+bool pair_ok(const ssd_scan_args& a) {
+  return a.H % 2 == 0 && (a.H / a.G) % 2 == 0 && a.P % 64 == 0 &&
+         (a.p_block == 0 || a.p_block == 64);
+}
 
-double plan_cost(const ssd_scan_args& a, int pb, int segc) {
+// Cost model in units of one 128-token chunk of a one-head 64-channel CTA in its steady
+// state (about 2 us).  The host sees only T and nseq (the lengths live on the device),
+// so sequences are taken as equally long.  One CTA per SM; a one-head CTA of channel
+// block PB that runs n chunks costs about kRamp + n (1 + PB/256) (the mask and C.B^T
+// work does not shrink with PB; kRamp is the pipeline fill of its first chunk), a pair
+// CTA kRamp + n kPairChunk for two heads.  A split adds the fix-up grid over the later
+// segments, one CTA per (segment, head, channel block) and one per SM at a time: a fixed
+// cost per wave (its launch, set-up and first tile), one chained step per segment before
+// it (the entering state) and per chunk 0.4 of a scan chunk when up to 96 fix-up CTAs
+// run at once, rising to 1.1 for a wave of 128 or more (each chunk reads and writes a y
+// tile; measured at 24 and at 128 heads).  (kFixBase also carries what a split costs the
+// scan grid itself beyond its chunks.)
+constexpr double kRamp = 3.0, kFixBase = 5.0, kFixPerSeg = 0.4;
+constexpr double kFixChunkLo = 0.4, kFixChunkHi = 1.1;
+constexpr double kPairChunk = 1.63;  // measured: a pair chunk takes 1.3x a one-head chunk
+
+double plan_cost(const ssd_scan_args& a, int hb, int pb, int segc) {
   const int sms = sm_count();
   const long long per = ((long long)a.T + a.nseq - 1) / a.nseq;
   const long long nch = std::max<long long>(1, (per + kScanChunk - 1) / kScanChunk);
   const long long nseg = segc > 0 ? (nch + segc - 1) / segc : 1;
   const long long chain = segc > 0 ? std::min<long long>(segc, nch) : nch;
-  const long long per_seg = (long long)a.H * (a.P / pb);
+  const long long per_seg = (long long)(a.H / hb) * (a.P / pb);
   const long long ctas = (long long)a.nseq * nseg * per_seg;
   const long long waves = (ctas + sms - 1) / sms;
-  double cost = (double)waves * (kRamp + chain * (1.0 + pb / 256.0));
+  const double per_chunk = hb == 2 ? kPairChunk : 1.0 + pb / 256.0;
+  double cost = (double)waves * (kRamp + chain * per_chunk);
   if (nseg > 1) {
-    const long long fix_ctas = (long long)a.nseq * (nseg - 1) * per_seg;
+    const long long fix_ctas = (long long)a.nseq * (nseg - 1) * a.H * (a.P / pb);
     const long long fix_waves = (fix_ctas + sms - 1) / sms;
-    cost += fix_waves * (kFixBase + kFixPerSeg * nseg + kFixPerChunk * chain);
+    const double busy =
+        std::min(1.0, std::max(0.0, (double)(std::min<long long>(fix_ctas, sms) - 96) / 32.0));
+    const double per_chunk = kFixChunkLo + (kFixChunkHi - kFixChunkLo) * busy;
+    cost += fix_waves * (kFixBase + kFixPerSeg * nseg + per_chunk * chain);
   }
   return cost;
 }
 
 constexpr int kMaxSplitSeqs = 1024;  // each CTA walks the sequence table to find its segment
 
-bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out) {
+// The cheapest plan under the cost model.  Splits are considered only when allowed, and
+// only those whose workspace fits in ws_limit bytes.
+bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out,
+               size_t ws_limit = SIZE_MAX) {
   ScanPlan best;
   double best_cost = 1e300;
   const long long per = ((long long)a.T + a.nseq - 1) / a.nseq;
   const int nch = (int)std::max<long long>(1, (per + kScanChunk - 1) / kScanChunk);
   const int lo = min_segc(a);
-  for (int pb : {64, 32, 16}) {
-    if (a.P % pb || (a.p_block && a.p_block != pb)) continue;
-    auto consider = [&](int segc) {
-      const double c = plan_cost(a, pb, segc);
-      if (c < best_cost - 1e-9) {
-        best_cost = c;
-        best.pb = pb;
-        best.segc = segc;
+  const int hb_lo = a.head_block == 2 ? 2 : 1, hb_hi = a.head_block == 1 ? 1 : 2;
+  for (int hb = hb_lo; hb <= hb_hi; ++hb) {
+    if (hb == 2 && !pair_ok(a)) continue;
+    for (int pb : {64, 32, 16}) {
+      if (a.P % pb || (a.p_block && a.p_block != pb) || (hb == 2 && pb != 64)) continue;
+      auto consider = [&](int segc) {
+        if (segc > 0 && ws_bytes_for(a, seg_capacity(a, segc)) > ws_limit) return;
+        const double c = plan_cost(a, hb, pb, segc);
+        if (c < best_cost - 1e-9) {
+          best_cost = c;
+          best.hb = hb;
+          best.pb = pb;
+          best.segc = segc;
+        }
+      };
+      if (a.seg_chunks >= 1) {
+        consider(std::max(a.seg_chunks, lo));
+      } else {
+        consider(0);
+        if (allow_split && a.seg_chunks == 0 && a.nseq <= kMaxSplitSeqs)
+          for (int segc = lo; segc < nch; ++segc) consider(segc);
       }
-    };
-    if (a.seg_chunks >= 1) {
-      consider(std::max(a.seg_chunks, lo));
-    } else {
-      consider(0);
-      if (allow_split && a.seg_chunks == 0 && a.nseq <= kMaxSplitSeqs)
-        for (int segc = lo; segc < nch; ++segc) consider(segc);
     }
   }
   if (best.pb == 0) return false;
@@ -1310,14 +1297,27 @@ bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out) {
   } else {
     best.nseg = a.nseq;
   }
-  if (best.nseg * a.H * (a.P / best.pb) > 0x7fffffffLL) return false;
+  if (best.nseg * (a.H / best.hb) * (a.P / best.pb) > 0x7fffffffLL) return false;
   *out = best;
+  return true;
+}
+
+// Opt in to the kernel's dynamic shared memory once per device.
+template <typename K>
+bool opt_in(K kernel, int bytes, std::atomic<bool>* done) {
+  const int dev = current_device();
+  if (done[dev].load(std::memory_order_acquire)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  done[dev].store(true, std::memory_order_release);
   return true;
 }
 
 template <int PB>
 ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t st) {
   using L = Layout<PB>;
+  const bool pair = plan.hb == 2;
   const int64_t xs = a.x_stride_t ? a.x_stride_t : (int64_t)a.H * a.P;
   const int64_t bs = a.B_stride_t ? a.B_stride_t : (int64_t)a.G * a.N;
   const int64_t cs = a.C_stride_t ? a.C_stride_t : (int64_t)a.G * a.N;
@@ -1333,21 +1333,18 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return SSD_ERR_CUDA;
   // dynamic shared memory above 48 KB is opted into once per kernel and device
-  static std::atomic<bool> attr_set[kMaxDevices];
-  const int dev = current_device();
-  if (!attr_set[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(scan_tc_kernel<PB, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(scan_tc_kernel<PB, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(scan_fixup_kernel<PB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             FixLayout<PB>::kSmemBytes) != cudaSuccess)
-      return SSD_ERR_CUDA;
-    attr_set[dev].store(true, std::memory_order_release);
-  }
+  static std::atomic<bool> set_one[kMaxDevices], set_one_split[kMaxDevices],
+      set_pair[kMaxDevices], set_pair_split[kMaxDevices], set_fix[kMaxDevices];
   const bool split = plan.segc > 0;
+  bool ok;
+  if (pair)
+    ok = split ? opt_in(scan_pair_kernel<true>, pair::kSmemBytes, set_pair_split)
+               : opt_in(scan_pair_kernel<false>, pair::kSmemBytes, set_pair);
+  else
+    ok = split ? opt_in(scan_tc_kernel<PB, true>, L::kSmemBytes, set_one_split)
+               : opt_in(scan_tc_kernel<PB, false>, L::kSmemBytes, set_one);
+  if (ok && split) ok = opt_in(scan_fixup_kernel<PB>, FixLayout<PB>::kSmemBytes, set_fix);
+  if (!ok) return SSD_ERR_CUDA;
   float* ws_h = split ? static_cast<float*>(a.workspace) : nullptr;
   float* ws_cs = split ? ws_h + ws_states_bytes(a, plan.nseg) / sizeof(float) : nullptr;
   TcParams prm;
@@ -1371,13 +1368,20 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   prm.npb = a.P / PB;
   prm.dt_softplus = a.dt_softplus;
   prm.segc = plan.segc;
-  const long long grid = plan.nseg * a.H * prm.npb;
-  if (!split) {
-    scan_tc_kernel<PB, false><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
-    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  const long long grid = plan.nseg * (a.H / plan.hb) * prm.npb;
+  if (pair) {
+    if (split)
+      scan_pair_kernel<true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
+    else
+      scan_pair_kernel<false><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
+  } else {
+    if (split)
+      scan_tc_kernel<PB, true><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
+    else
+      scan_tc_kernel<PB, false><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
   }
-  scan_tc_kernel<PB, true><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
   if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+  if (!split) return SSD_OK;
   FixParams fp;
   fp.A = a.A;
   fp.cu = a.cu_seqlens;
@@ -1396,7 +1400,7 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   // programmatic stream serialisation: the fix-up grid may start while the scan grid
   // drains; it waits for the scan's completion before it reads the scan's outputs
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)(plan.nseg * a.H * prm.npb));
   cfg.blockDim = dim3(kFixThreads);
   cfg.dynamicSmemBytes = FixLayout<PB>::kSmemBytes;
   cfg.stream = st;
@@ -1429,16 +1433,19 @@ bool scan_tc_supported(const ssd_scan_args& a) {
   return plan_scan(a, false, &plan);
 }
 
-size_t scan_tc_workspace_size(const ssd_scan_args& a) {
+size_t scan_tc_workspace_size(const ssd_scan_args& a, size_t ws_limit) {
   if (!scan_tc_supported(a) || a.seg_chunks < 0) return 0;
   ScanPlan plan;
-  if (!plan_scan(a, true, &plan)) return 0;
+  if (!plan_scan(a, true, &plan, ws_limit)) return 0;
   return plan.ws_bytes;
 }
 
-ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t st) {
+ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t st, size_t ws_limit) {
   ScanPlan plan;
-  if (!plan_scan(a, a.seg_chunks >= 0, &plan)) return SSD_ERR_UNSUPPORTED;
+  if (!plan_scan(a, a.seg_chunks >= 0, &plan, ws_limit)) {
+    if (a.seg_chunks >= 1) return SSD_ERR_UNSUPPORTED;
+    if (!plan_scan(a, false, &plan)) return SSD_ERR_UNSUPPORTED;
+  }
   if (plan.segc > 0) {
     const bool ws_ok = a.workspace && ((uintptr_t)a.workspace & 255u) == 0 &&
                        a.workspace_bytes >= plan.ws_bytes;

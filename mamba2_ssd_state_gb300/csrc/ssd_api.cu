@@ -27,6 +27,7 @@ ssd_status validate_scan(const ssd_scan_args* a) {
   if (a->p_block != 0 && a->p_block != 16 && a->p_block != 32 && a->p_block != 64)
     return SSD_ERR_INVALID_ARG;
   if (a->seg_chunks < -1) return SSD_ERR_INVALID_ARG;
+  if (a->head_block < 0 || a->head_block > 2) return SSD_ERR_INVALID_ARG;
   if (a->workspace_bytes > 0 && !a->workspace) return SSD_ERR_INVALID_ARG;
   if (a->nseq > 65535 || a->H > 65535) return SSD_ERR_UNSUPPORTED;  // grid limits
   return SSD_OK;
@@ -75,15 +76,17 @@ ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_stream_t stre
   const bool tc_ok = scan_tc_supported(a);
   if (a.impl == SSD_IMPL_TC || (a.impl == SSD_IMPL_AUTO && tc_ok)) {
     if (!tc_ok) return SSD_ERR_UNSUPPORTED;
-    const size_t need = scan_tc_workspace_size(a);
-    if (need > scan_static_scratch_bytes()) return SSD_ERR_UNSUPPORTED;  // before any launch
+    const size_t cap = scan_static_scratch_bytes();
+    // an explicit split must fit the array; the automatic plan keeps to it
+    if (a.seg_chunks >= 1 && scan_tc_workspace_size(a) > cap) return SSD_ERR_UNSUPPORTED;
+    const size_t need = scan_tc_workspace_size(a, cap);
     ssd_scan_args b = a;
     if (need > 0) {
       b.workspace = scan_static_scratch();
       if (!b.workspace) return SSD_ERR_CUDA;
-      b.workspace_bytes = scan_static_scratch_bytes();
+      b.workspace_bytes = cap;
     }
-    return launch_scan_tc(b, st);
+    return launch_scan_tc(b, st, cap);
   }
   if (a.N > 256) return SSD_ERR_UNSUPPORTED;
   return launch_scan_simt(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdint>
+
 #include "../../include/ssd.h"
 
 namespace ssd {
@@ -41,9 +43,10 @@ cudaError_t launch_scan_simt(const ssd_scan_args& a, cudaStream_t s);
 // Tensor-core scan: supported shapes, the workspace its plan wants (0 = no split) and the
 // launch (SSD_ERR_UNSUPPORTED for shapes it cannot take, SSD_ERR_INVALID_ARG for a forced
 // split without a large enough workspace).
+// ws_limit caps the workspace of the splits the planner may choose (SIZE_MAX: no cap).
 bool scan_tc_supported(const ssd_scan_args& a);
-size_t scan_tc_workspace_size(const ssd_scan_args& a);
-ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s);
+size_t scan_tc_workspace_size(const ssd_scan_args& a, size_t ws_limit = SIZE_MAX);
+ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s, size_t ws_limit = SIZE_MAX);
 
 // Decode-side ops (decode.cu).
 bool decode_n_supported(int N);

@@ -43,7 +43,8 @@ class ScanArgs(ctypes.Structure):
                 ("nseq", _i32), ("T", _i32), ("H", _i32), ("P", _i32), ("G", _i32),
                 ("N", _i32), ("chunk_size", _i32), ("act_dtype", ctypes.c_int), ("y", _vp),
                 ("final_states", _vp), ("d_status", _vp), ("impl", _i32), ("p_block", _i32),
-                ("seg_chunks", _i32), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+                ("seg_chunks", _i32), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+                ("head_block", _i32)]
 
 
 class UpdateArgs(ctypes.Structure):
@@ -158,19 +159,20 @@ def _raise(rc, where):
 def chunk_scan(x, dt, A, B, C, *, cu_seqlens, chunk_size, D=None, dt_bias=None,
                dt_softplus=True, initial_states=None, has_initial_state=None, y=None,
                final_states=None, return_final_states=True, status=None, impl="auto",
-               p_block=0, seg_chunks=0, workspace=None, stream=None):
+               p_block=0, seg_chunks=0, workspace=None, stream=None, head_block=0):
     """Mamba2 chunked SSD scan over packed sequences (see ssd_chunk_scan in ssd.h).
 
     x [T,H,P], B/C [T,G,N] (bf16 or fp32, token stride may exceed the dense size);
     dt [T,H], A/D/dt_bias [H], initial_states [nseq,H,P,N] fp32; cu_seqlens int32
     [nseq+1] on the device.  seg_chunks: 0 = the library decides whether to split long
     sequences (it then gets a workspace from torch's allocator unless one is passed),
-    -1 = never, k >= 1 = segments of k 128-token chunks.  Returns (y, final_states)."""
+    -1 = never, k >= 1 = segments of k 128-token chunks.  head_block: heads per CTA of the
+    tensor-core path (0 = the library decides, 1, or 2).  Returns (y, final_states)."""
     lib = load_library()
     a, y, final_states, _ws = _scan_args(
         lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus, initial_states,
         has_initial_state, y, final_states, return_final_states, status, impl, p_block,
-        seg_chunks, workspace)
+        seg_chunks, workspace, head_block)
     _raise(lib.ssd_chunk_scan(ctypes.byref(a), _stream(stream)), "ssd_chunk_scan")
     return y, final_states
 
@@ -179,7 +181,8 @@ def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_s
                           group_size, eps=1e-5, D=None, dt_bias=None, dt_softplus=True,
                           initial_states=None, has_initial_state=None, y=None, out=None,
                           final_states=None, return_final_states=True, status=None,
-                          impl="auto", p_block=0, seg_chunks=0, workspace=None, stream=None):
+                          impl="auto", p_block=0, seg_chunks=0, workspace=None, stream=None,
+                          head_block=0):
     """The scan of chunk_scan followed by the gated RMSNorm of gated_rmsnorm over its
     output, in one call (ssd_chunk_scan_gated_norm in ssd.h).  z [T,H*P] (or None: no
     gate), norm_weight [H*P].  y (optional) receives the pre-norm output; without it the
@@ -200,7 +203,7 @@ def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_s
     a, y, final_states, _ws = _scan_args(
         lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus, initial_states,
         has_initial_state, y if y is not None else out.view(T, H, P), final_states,
-        return_final_states, status, impl, p_block, seg_chunks, workspace)
+        return_final_states, status, impl, p_block, seg_chunks, workspace, head_block)
     _raise(lib.ssd_chunk_scan_gated_norm(ctypes.byref(a), _ptr(z), _ptr(norm_weight),
                                          _act(norm_weight), int(group_size), float(eps),
                                          _ptr(out), _stream(stream)),
@@ -210,7 +213,7 @@ def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_s
 
 def _scan_args(lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus,
                initial_states, has_initial_state, y, final_states, return_final_states, status,
-               impl, p_block, seg_chunks, workspace):
+               impl, p_block, seg_chunks, workspace, head_block=0):
     """ssd_scan_args for one scan call, with the outputs (and a workspace from torch's
     allocator, when the plan wants one and none was passed) made where missing."""
     T, H, P = x.shape
@@ -254,7 +257,7 @@ def _scan_args(lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softp
     a.act_dtype = act
     a.y, a.final_states, a.d_status = _ptr(y), _ptr(final_states), _ptr(status)
     a.impl, a.p_block = IMPL[impl], int(p_block)
-    a.seg_chunks = int(seg_chunks)
+    a.seg_chunks, a.head_block = int(seg_chunks), int(head_block)
     if workspace is None and a.seg_chunks >= 0:
         nbytes = lib.ssd_chunk_scan_workspace_size(ctypes.byref(a))
         if nbytes:
@@ -266,7 +269,7 @@ def _scan_args(lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softp
 
 
 def chunk_scan_workspace_size(x, B, C, *, cu_seqlens, chunk_size, impl="auto", p_block=0,
-                              seg_chunks=0):
+                              seg_chunks=0, head_block=0):
     """Bytes of workspace chunk_scan would want for these shapes (0 = it would not split;
     ssd_chunk_scan_workspace_size in ssd.h).  y is taken as a dense aligned tensor."""
     lib = load_library()
@@ -282,6 +285,7 @@ def chunk_scan_workspace_size(x, B, C, *, cu_seqlens, chunk_size, impl="auto", p
     a.nseq, a.T, a.H, a.P, a.G, a.N = cu_seqlens.shape[0] - 1, T, H, P, G, N
     a.chunk_size, a.act_dtype = int(chunk_size), _act(x)
     a.impl, a.p_block, a.seg_chunks = IMPL[impl], int(p_block), int(seg_chunks)
+    a.head_block = int(head_block)
     return int(lib.ssd_chunk_scan_workspace_size(ctypes.byref(a)))
 
 

@@ -17,7 +17,8 @@ def dev(t, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(t.values)).to(device=device, dtype=dtype)
 
 
-def scan_gpu(s, impl="auto", p_block=0, final=True, chunk_size=None, D=True, seg_chunks=0):
+def scan_gpu(s, impl="auto", p_block=0, final=True, chunk_size=None, D=True, seg_chunks=0,
+             head_block=0):
     status = ssd.new_status()
     hi = None if s.has_initial_state is None else torch.from_numpy(s.has_initial_state).cuda()
     y, fs = ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C),
@@ -26,7 +27,7 @@ def scan_gpu(s, impl="auto", p_block=0, final=True, chunk_size=None, D=True, seg
                            D=dev(s.D) if D else None, dt_bias=dev(s.dt_bias),
                            initial_states=dev(s.initial_states), has_initial_state=hi,
                            return_final_states=final, status=status, impl=impl,
-                           p_block=p_block, seg_chunks=seg_chunks)
+                           p_block=p_block, seg_chunks=seg_chunks, head_block=head_block)
     rc, bits = ssd.read_status(status)
     torch.cuda.synchronize()
     yf = y.float().cpu().numpy()
@@ -53,7 +54,7 @@ def scan_oracle(s, heads=None, with_abs=False, D=True):
 
 
 def scan_args_struct(x, dt, A, B, C, cu, chunk_size, *, D=None, dt_bias=None, init=None, y=None,
-          fs=None, status=None, seg_chunks=0):
+          fs=None, status=None, seg_chunks=0, head_block=0):
     """ssd_scan_args for the given tensors (the marshalling of ssd.chunk_scan), for tests
     that call an entry point of the C ABI directly."""
     T, H, P = x.shape
@@ -71,5 +72,5 @@ def scan_args_struct(x, dt, A, B, C, cu, chunk_size, *, D=None, dt_bias=None, in
     a.chunk_size = chunk_size
     a.act_dtype = ssd._act(x)
     a.y, a.final_states, a.d_status = ssd._ptr(y), ssd._ptr(fs), ssd._ptr(status)
-    a.seg_chunks = seg_chunks
+    a.seg_chunks, a.head_block = seg_chunks, head_block
     return a

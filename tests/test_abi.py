@@ -71,7 +71,7 @@ def _scan_args(**kw):
     dict(struct_size=8), dict(A=None), dict(cu_seqlens=None), dict(x=None), dict(nseq=0),
     dict(H=3), dict(G=0), dict(P=0), dict(N=0), dict(chunk_size=0), dict(chunk_size=257),
     dict(act_dtype=7), dict(x_stride_t=10), dict(B_stride_t=5), dict(impl=9), dict(p_block=48),
-    dict(seg_chunks=-2), dict(workspace_bytes=256),
+    dict(seg_chunks=-2), dict(workspace_bytes=256), dict(head_block=3), dict(head_block=-1),
 ])
 def test_scan_rejects_bad_arguments(lib, bad):
     a = _scan_args(**bad)
@@ -122,14 +122,22 @@ def test_scan_workspace_size(lib):
     assert size(seg_chunks=-1) == 0                       # never split
     assert size(seg_chunks=4, impl=1) == 0                # SIMT path: no workspace
     assert size(seg_chunks=4, act_dtype=ssd.SSD_F32) == 0  # not a tensor-core shape
-    # the planner cuts two 2048-token sequences into 6-chunk segments (channel block 64:
-    # 2 x 3 x 24 = 144 CTAs, one wave), keeps a Nemotron-H-shaped batch whole, and
-    # splits one sequence of 16384 tokens
-    assert size() == r256((2 + (4096 + 127 * 2) // (128 * 6)) * 24 * 64 * 128 * 4
-                          + 4096 * 24 * 4)
-    assert size(nseq=4, T=16384, H=128, G=8) == 0
+    # one head per CTA, the planner cuts two 2048-token sequences into 6-chunk segments
+    # (channel block 64: 2 x 3 x 24 = 144 CTAs, one wave), keeps a Nemotron-H-shaped
+    # batch whole, and splits one sequence of 16384 tokens
+    assert size(head_block=1) == r256((2 + (4096 + 127 * 2) // (128 * 6)) * 24 * 64 * 128 * 4
+                                      + 4096 * 24 * 4)
+    assert size(nseq=4, T=16384, H=128, G=8, head_block=1) == 0
     auto = size(nseq=1, T=16384)
     assert auto > 0 and auto % 256 == 0
+    # with head pairs allowed, the planner keeps the 6-chunk segments of one head per CTA
+    # for the two 2048-token sequences (its cheapest plan there), and keeps the
+    # Nemotron-H-shaped varlen batch and single 16K / 64K-token Nemotron-H sequences
+    # whole (128 heads: the fix-up of a split would move y twice for every later segment)
+    assert size() == size(head_block=1)
+    assert size(nseq=4, T=16384, H=128, G=8) == 0
+    assert size(nseq=1, T=16384, H=128, G=8) == 0
+    assert size(nseq=1, T=65536, H=128, G=8) == 0
     assert lib.ssd_chunk_scan_workspace_size(None) == 0
 
 

@@ -48,16 +48,22 @@ def test_fp32_varlen_edges(N):
 SEQS = [300, 129, 1, 64, 700, 0, 128, 127, 255]
 
 
-@pytest.mark.parametrize("p_block", [16, 32, 64])
+# The tensor-core kernels: one head per CTA at channel blocks 16, 32 and 64, and the
+# head-pair kernel (two heads of one group per CTA, 64 channels each).
+TC_KERNELS = [(16, 1), (32, 1), (64, 1), (64, 2)]
+
+
+@pytest.mark.parametrize("p_block,head_block", TC_KERNELS)
 @pytest.mark.parametrize("chunk", [64, 128, 256])
-def test_bf16_tensor_core_parity(p_block, chunk):
+def test_bf16_tensor_core_parity(p_block, head_block, chunk):
     s = I.make_scan_inputs(SEQS, H=4, P=64, G=2, N=128, chunk_size=chunk, act="bf16",
                            seed=103, init=[1, 0, 1, 1, 0, 1, 0, 1, 1])
-    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block)
+    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block, head_block=head_block)
     assert bits == 0
     yr, fr = scan_oracle(s)
-    check_bf16(f"tc pb={p_block} Q={chunk} y", y, yr)
-    check_bf16(f"tc pb={p_block} Q={chunk} final", fs, fr)
+    tag = f"tc pb={p_block} hb={head_block} Q={chunk}"
+    check_bf16(f"{tag} y", y, yr)
+    check_bf16(f"{tag} final", fs, fr)
 
 
 def test_bf16_simt_parity():
@@ -121,20 +127,21 @@ SEG_SEQS = [700, 129, 1, 0, 300, 1000, 257, 128, 385]
 SEG_INIT = [1, 0, 1, 1, 0, 1, 1, 0, 1]
 
 
-@pytest.mark.parametrize("p_block", [16, 32, 64])
+@pytest.mark.parametrize("p_block,head_block", TC_KERNELS)
 @pytest.mark.parametrize("seg", [1, 2, 3])
-def test_bf16_segmented_parity(p_block, seg):
+def test_bf16_segmented_parity(p_block, head_block, seg):
     s = I.make_scan_inputs(SEG_SEQS, H=4, P=64, G=2, N=128, chunk_size=256, act="bf16",
                            seed=141, init=SEG_INIT)
-    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block, seg_chunks=seg)
+    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block, seg_chunks=seg,
+                           head_block=head_block)
     assert bits == 0
     yr, fr = scan_oracle(s)
-    check_bf16(f"seg={seg} pb={p_block} y", y, yr)
-    check_bf16(f"seg={seg} pb={p_block} final", fs, fr)
+    check_bf16(f"seg={seg} pb={p_block} hb={head_block} y", y, yr)
+    check_bf16(f"seg={seg} pb={p_block} hb={head_block} final", fs, fr)
     # the empty sequence still returns its initial state, untouched by the chaining
     np.testing.assert_array_equal(fs[3], s.initial_states.values[3])
     # and the split agrees with the unsplit chain
-    y1, f1, _ = scan_gpu(s, impl="tc", p_block=p_block, seg_chunks=-1)
+    y1, f1, _ = scan_gpu(s, impl="tc", p_block=p_block, seg_chunks=-1, head_block=head_block)
     check_bf16(f"seg={seg} vs unsplit y", y, y1)
     check_bf16(f"seg={seg} vs unsplit final", fs, f1)
 
@@ -166,6 +173,54 @@ def test_segmented_needs_workspace():
     y, _ = ssd.chunk_scan(*args, workspace=small, **kw)
     yr, _ = scan_oracle(s)
     check_bf16("unsplit fallback y", y.float().cpu().numpy(), yr)
+
+
+@pytest.mark.parametrize("seg", [-1, 1])
+def test_pair_one_head_A_not_negative(seg):
+    """A head pair whose second head fails the sign test: that head's y and final state
+    are zero and the status bit is set, while its partner (same CTA, same C.B^T and the
+    same batched products) still matches the oracle."""
+    s = I.make_scan_inputs([600, 130], H=4, P=64, G=2, N=128, chunk_size=128, act="bf16",
+                           seed=147, init="all")
+    A = s.A.values.copy()
+    A[1] = float("nan")
+    A[2] = 0.0
+    s.A = I.Tensor(A, "f32")
+    y, fs, bits = scan_gpu(s, impl="tc", head_block=2, seg_chunks=seg)
+    assert bits & ssd.DEV_A_NOT_NEG
+    for h in (1, 2):
+        assert np.all(y[:, h] == 0) and np.all(fs[:, h] == 0)
+    yr, fr = scan_oracle(s, heads=[0, 3])
+    check_bf16(f"pair bad heads seg={seg} y", y[:, [0, 3]], yr)
+    check_bf16(f"pair bad heads seg={seg} final", fs[:, [0, 3]], fr)
+
+
+def test_pair_headdim_128():
+    """P = 128: each head pair runs as two CTAs, one per 64-channel block."""
+    s = I.make_scan_inputs([300, 77, 513], H=4, P=128, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=149, init=[1, 0, 1])
+    y, fs, bits = scan_gpu(s, impl="tc", head_block=2)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("pair P=128 y", y, yr)
+    check_bf16("pair P=128 final", fs, fr)
+
+
+@pytest.mark.parametrize("shape", [dict(H=3, G=1, P=64), dict(H=6, G=2, P=64),
+                                   dict(H=4, G=2, P=32)])
+def test_pair_unsupported_shapes(shape):
+    """Two heads per CTA need H and H/G even and 64-channel blocks: other shapes are
+    refused with SSD_ERR_UNSUPPORTED when the pair kernel is forced, and run one head per
+    CTA when the library chooses."""
+    s = I.make_scan_inputs([200], N=128, chunk_size=128, act="bf16", seed=151, init="all",
+                           **shape)
+    with pytest.raises(ssd.SsdError) as e:
+        scan_gpu(s, impl="tc", head_block=2)
+    assert e.value.code == 2
+    y, fs, bits = scan_gpu(s, impl="tc")
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16(f"auto {shape} y", y, yr)
 
 
 @pytest.mark.parametrize("impl", ["tc", "simt"])
@@ -222,16 +277,28 @@ def test_mamba2_130m_layer_full(seg):
     check_bf16(f"mamba2_130m seg={seg} final", fs, fr)
 
 
-@pytest.mark.parametrize("seg", [0, 4])
-def test_nemotron_h_varlen_sampled_heads(seg):
-    """4 packed sequences (8192, 3000, 517, 4675), H=128, G=8: heads from every group."""
+def test_nemotron_h_varlen_all_heads():
+    """4 packed sequences (8192, 3000, 517, 4675), H=128, G=8, as the library plans it
+    (the launch the benchmark times): every head, every token, every final state."""
     s = I.scan_workload("nemotron_h_varlen")
-    y, fs, bits = scan_gpu(s, seg_chunks=seg)
+    y, fs, bits = scan_gpu(s)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("nemotron_h y", y, yr)
+    check_bf16("nemotron_h final", fs, fr)
+
+
+@pytest.mark.parametrize("seg,head_block", [(4, 0), (-1, 1), (4, 1)])
+def test_nemotron_h_varlen_sampled_heads(seg, head_block):
+    """The same batch split into 4-chunk segments and with one head per CTA: heads from
+    every group."""
+    s = I.scan_workload("nemotron_h_varlen")
+    y, fs, bits = scan_gpu(s, seg_chunks=seg, head_block=head_block)
     assert bits == 0
     heads = [0, 17, 38, 63, 64, 90, 111, 127]
     yr, fr = scan_oracle(s, heads=heads)
-    check_bf16("nemotron_h sampled y", y[:, heads], yr)
-    check_bf16("nemotron_h sampled final", fs[:, heads], fr)
+    check_bf16(f"nemotron_h seg={seg} hb={head_block} y", y[:, heads], yr)
+    check_bf16(f"nemotron_h seg={seg} hb={head_block} final", fs[:, heads], fr)
 
 
 def test_single_long_sequence_planned_split():
