@@ -1,16 +1,21 @@
 """Benchmark of the Mamba2 SSD hot path on GB300.
 
-One step = one pass of the whole path over one batch of synthetic input shaped like a
-Mamba2-130M layer: the chunked scan over 2 sequences x 2048 tokens (H=24, P=64, G=1,
-N=128, chunk 256, bf16 activations, fp32 initial states), the gated RMSNorm of its output
-(d_inner 1536, one group), and one decode token for both requests through the pooled
-state update.  Inputs are resident in HBM; L2 (129 MB, larger than the step's inputs) is
-flushed between timed steps (512 MB write, then a 512 MB read so no dirty line is left to
-write back), outside the timed events.
+One step = one pass of the whole hot path over one batch of synthetic input shaped like a
+Nemotron-H Mamba2 layer: 4 packed prefill sequences of [8192, 3000, 517, 4675] tokens
+(16384 tokens, H=128, P=64, G=8, N=128, chunk 128, bf16 activations, fp32 initial states
+on sequences 0 and 2) through the chunked scan with D skip and the silu-gated RMSNorm
+(8 groups of 1024) in one call, and the next decode token of the same 4 requests through
+the pooled state update on a second stream.  `value` counts the prefill tokens only.
+Inputs are resident in HBM; L2 (129 MB, smaller than the step's 0.9 GB of inputs and
+outputs) is flushed between timed steps anyway (512 MB write, then a 512 MB read so no
+dirty line is left to write back), outside the timed events.
 
 Prints one JSON line (rank 0).  Also measured in the same run and reported as extra keys:
-the decode state update on a 512-slot [128, 64, 128] fp32 pool at batch 256 (HBM GB/s),
-and the scan on the Nemotron-H-shaped varlen prefill (16384 tokens, H=128, G=8).
+the Mamba2-130M-shaped layer step, the gated norm alone at the Nemotron-H shape, the
+decode state update on a 512-slot [128, 64, 128] fp32 pool at batch 256 (HBM GB/s), the
+decode layer step, the multi-token update beside the HBM write-only rate, the slot copy,
+one long sequence on few heads, and the prefill layer path at Nemotron-H shapes (single
+sequences of 1K..64K tokens, and a mixed batch with a concurrent decode).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -33,8 +38,11 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "mamba2_130m"
+WORKLOAD = "nemotron_h_varlen"
 METRIC = "Mamba2 SSD prefill tokens/s; decode state-update HBM GB/s vs peak"
+KERNEL_CHUNK = 128  # tokens per chunk of the tensor-core scan kernels (their MMA tile)
+SCAN_SRCS = ["scan_tc.cu", "scan_pair.cuh", "tc_ptx.cuh", "ssd_internal.cuh",
+             "scan_segments.cuh"]
 
 
 def load_peaks():
@@ -45,38 +53,51 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def scan_traffic_from_profile():
-    """DRAM bytes per launch of the scan on this workload from the committed ncu summary,
-    if the kernel sources still hash to what was profiled; else None."""
+def scan_sources_sha256():
     import hashlib
+
+    h = hashlib.sha256()
+    for f in SCAN_SRCS:
+        h.update(open(os.path.join(ROOT, "mamba2_ssd_state_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def scan_traffic_from_profile(name):
+    """DRAM bytes per launch of the scan from the committed ncu summary profiles/<name>,
+    if the kernel sources still hash to what was profiled; else None."""
     import re
 
-    prof = os.path.join(ROOT, "profiles", "scan_tc_mamba2_130m.md")
-    srcs = ["scan_tc.cu", "tc_ptx.cuh", "ssd_internal.cuh", "scan_segments.cuh"]
     try:
-        txt = open(prof).read()
-        h = hashlib.sha256()
-        for f in srcs:
-            h.update(open(os.path.join(ROOT, "mamba2_ssd_state_gb300", "csrc", f), "rb").read())
+        txt = open(os.path.join(ROOT, "profiles", name)).read()
+        digest = scan_sources_sha256()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", txt)
     m_traffic = re.search(r"traffic_bytes_per_launch\s*\|\s*(\d+)", txt)
-    if not m_hash or not m_traffic or m_hash.group(1) != h.hexdigest():
+    if not m_hash or not m_traffic or m_hash.group(1) != digest:
         return None
     return int(m_traffic.group(1))
 
 
-def scan_bytes(T, H, P, G, N, nseq, init=True, final=True, act_bytes=2):
+def scan_bytes(T, H, P, G, N, nseq, n_init=None, final=True, act_bytes=2):
     """Algorithmic HBM bytes of one scan launch: x and y, B and C, dt, per-head params,
-    initial and final states (intermediate chunk states are not counted)."""
+    the initial states that are read (n_init sequences; all when None) and the final
+    states (intermediate chunk states are not counted)."""
     b = T * H * P * act_bytes * 2 + T * G * N * act_bytes * 2 + T * H * 4 + H * 4 * 3
     b += (nseq + 1) * 4
-    if init:
-        b += nseq * H * P * N * 4
+    b += (nseq if n_init is None else n_init) * H * P * N * 4
     if final:
         b += nseq * H * P * N * 4
     return b
+
+
+def layer_bytes(T, H, P, G, N, nseq=0, n_init=0, final=False):
+    """Algorithmic bytes of the prefill layer path (scan, D skip, gated norm) in bf16: x, z
+    and out 2HP each, B and C 2GN each and dt 4H per token, plus the norm weight and, when
+    asked, the initial states read and the final states written; y is an intermediate
+    and not counted."""
+    b = T * (6 * H * P + 4 * G * N + 4 * H) + 2 * H * P
+    return b + (n_init + (nseq if final else 0)) * H * P * N * 4
 
 
 def update_bytes(active, batch, H, P, G, N, act_bytes=2):
@@ -153,6 +174,28 @@ class L2Flush:
         self.acc += self.r.sum()
 
 
+def graph_of(torch, fn):
+    """fn() captured in a CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def timed_replays(torch, stream, l2, replay, n):
+    """Device time (ms) of n replays, each after an L2 flush outside its events."""
+    ts = []
+    for _ in range(n):
+        l2.flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return ts
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -173,21 +216,24 @@ def run_ours(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
 
     w = I.WORKLOADS[WORKLOAD]
-    # data parallel: rank r processes its own batch of the workload (sequences r*2, r*2+1
-    # of the global batch), drawn with its own seed; no collective on the data path
+    # data parallel: rank r processes its own batch of the workload, drawn with its own
+    # seed; no collective on the data path
     s = I.scan_workload(WORKLOAD, seed=w["seed"] + 17 * rank)
     H, P, G, N, T, nseq = s.H, s.P, s.G, s.N, s.T, s.nseq
-    d = H * P
+    d, group = H * P, w["norm_group"]
     x, dt, A, B, C, Dp, bias = (T_(s.x), T_(s.dt), T_(s.A), T_(s.B), T_(s.C), T_(s.D),
                                 T_(s.dt_bias))
     init = T_(s.initial_states)
+    hi = torch.from_numpy(s.has_initial_state).to(dev)
+    n_init = int(np.sum(s.has_initial_state))
     cu = torch.from_numpy(s.cu_seqlens).to(dev)
-    nrm = I.make_norm_inputs(T, d, w["norm_group"], act="bf16", seed=w["seed"] + 50)
+    nrm = I.make_norm_inputs(T, d, group, act="bf16", seed=w["seed"] + 50)
     z, wt = T_(nrm.z), T_(nrm.weight)
     y = torch.empty((T, H, P), dtype=torch.bfloat16, device=dev)
     fs = torch.empty((nseq, H, P, N), dtype=torch.float32, device=dev)
     out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-    # decode of both requests after their prefill: slots 0 and 1 of a 2-slot pool
+    # the next decode token of the nseq requests: their pool slots hold the final states
+    # of the prefill after the first warm-up step
     pool = torch.zeros((nseq, H, P, N), dtype=torch.float32, device=dev)
     upd = I.make_update_inputs(nseq, list(range(nseq)), H, P, G, N, act="bf16",
                                seed=w["seed"] + 60)
@@ -198,43 +244,42 @@ def run_ours(args, rank, world, local_rank):
     l2 = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
+    def scan_call():
         ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp,
-                       dt_bias=bias, initial_states=init, y=y, final_states=fs, status=status)
-        if ev:
-            ev[1].record(stream)
-        ssd.gated_rmsnorm(y.view(T, d), z, wt, group_size=w["norm_group"], eps=1e-5, out=out)
-        if ev:
-            ev[2].record(stream)
-        ssd.state_update(pool, uidx, ux, udt, A, uB, uC, D=Dp, dt_bias=bias, y=uy,
-                         status=status)
-        if ev:
-            ev[3].record(stream)
+                       dt_bias=bias, initial_states=init, has_initial_state=hi, y=y,
+                       final_states=fs, status=status)
 
-    def layer_prefill(stream_=None, inp=None, out_=None):
+    def norm_call():
+        ssd.gated_rmsnorm(y.view(T, d), z, wt, group_size=group, eps=1e-5, out=out)
+
+    def decode_call(st=None, inp=None):
+        i = inp or dict(ux=ux, udt=udt, uB=uB, uC=uC)
+        ssd.state_update(pool, uidx, i["ux"], i["udt"], A, i["uB"], i["uC"], D=Dp, dt_bias=bias,
+                         y=uy, status=status, stream=st)
+
+    def layer_prefill(st=None, inp=None, out_=None):
         """The prefill half of the layer in one call: scan, then the gated norm launched as
-        its programmatic dependent, normalising in place in out (the pre-norm y is not
-        kept)."""
+        its programmatic dependent, normalising in place in out."""
         i = inp or dict(x=x, dt=dt, B=B, C=C, init=init, z=z)
         ssd.chunk_scan_gated_norm(i["x"], i["dt"], A, i["B"], i["C"], i["z"], wt, cu_seqlens=cu,
-                                  chunk_size=s.chunk_size, group_size=w["norm_group"],
-                                  eps=1e-5, D=Dp, dt_bias=bias, initial_states=i["init"],
+                                  chunk_size=s.chunk_size, group_size=group, eps=1e-5, D=Dp,
+                                  dt_bias=bias, initial_states=i["init"], has_initial_state=hi,
                                   out=out if out_ is None else out_, final_states=fs,
-                                  status=status, stream=stream_)
+                                  status=status, stream=st)
 
     # the scan is one launch, or two when the library splits the sequences into segments
-    # (scan, fix-up)
     scan_split = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu,
                                                chunk_size=s.chunk_size) > 0
     launches_per_step = (2 if scan_split else 1) + 2
     for i in range(max(args.warmup, 3)):
         l2.flush()
-        step()
+        scan_call()
+        norm_call()
+        decode_call()
         layer_prefill()
         if i == 0:
-            pool.copy_(fs)   # the decode continues the two requests just prefilled
+            torch.cuda.synchronize()
+            pool.copy_(fs)   # the decode continues the requests just prefilled
     torch.cuda.synchronize()
     rc, bits = ssd.read_status(status)
     if bits:
@@ -242,27 +287,25 @@ def run_ours(args, rank, world, local_rank):
 
     # The timed step is one CUDA graph of its launches (the way a serving engine runs a
     # layer): no host work and no launch gaps.  The decode token depends on neither this
-    # step's scan nor its norm, so it runs on a second stream in the graph, on the SMs
-    # the scan's chains leave free.
+    # step's scan nor its norm, so it runs on a second stream in the graph.
     s_dec = torch.cuda.Stream(device=dev)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         cap = torch.cuda.current_stream()
         s_dec.wait_stream(cap)
         with torch.cuda.stream(s_dec):
-            ssd.state_update(pool, uidx, ux, udt, A, uB, uC, D=Dp, dt_bias=bias, y=uy,
-                             status=status)
+            decode_call()
         layer_prefill()
         cap.wait_stream(s_dec)
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
-    # the timed region is milliseconds long: keep the GPU under the same load for a
-    # second first, so the clock samples (100 ms apart) cover the state it is timed in
+    # keep the GPU under the same load for a second first, so that the clock samples
+    # (100 ms apart) cover the state it is timed in
     t_load = time.perf_counter()
     while time.perf_counter() - t_load < 1.0:
-        for _ in range(50):
+        for _ in range(10):
             l2.flush()
             graph.replay()
         torch.cuda.synchronize()
@@ -282,68 +325,53 @@ def run_ours(args, rank, world, local_rank):
     ck = clocks.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = shard.max_over_ranks(sum(step_ms), dev)
-    # per-op split of a step: the same step launched op by op, events between the ops
-    # (not part of `value`; launch gaps make these slightly longer than inside the graph)
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        l2.flush()
-        step(evb[k])
-    torch.cuda.synchronize()
-    scan_ms = [e[0].elapsed_time(e[1]) for e in evb]
-    norm_ms = [e[1].elapsed_time(e[2]) for e in evb]
-    upd_ms = [e[2].elapsed_time(e[3]) for e in evb]
-    # the scan + norm call alone (the norm a dependent launch of the scan)
-    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        l2.flush()
-        evf[k][0].record(stream)
-        layer_prefill()
-        evf[k][1].record(stream)
-    torch.cuda.synchronize()
-    fused_ms = [e[0].elapsed_time(e[1]) for e in evf]
-    tokens_per_step = T + nseq
+    tokens_per_step = T       # prefill tokens; the decode tokens are not counted
     value = tokens_per_step * world * args.steps / (total_ms / 1e3)
 
-    sbytes = scan_bytes(T, H, P, G, N, nseq)
-    # the scan's device time for the roofline: the scan call alone captured in a graph and
-    # replayed after an L2 flush (outside the events), so that no host work of the
-    # binding falls inside the events (op by op it can: the GPU may sit idle while the
-    # next launch is prepared)
-    g_scan = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_scan):
-        ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp,
-                       dt_bias=bias, initial_states=init, y=y, final_states=fs, status=status)
-    scan_dev_ms = []
-    for k in range(args.steps):
-        l2.flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g_scan.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        scan_dev_ms.append(e0.elapsed_time(e1))
-    scan_avg = sum(scan_dev_ms) / len(scan_dev_ms)
-    scan_kernels = "scan_tc_kernel + scan_fixup_kernel" if scan_split else "scan_tc_kernel"
-    roof = {"bound": "hbm", "kernel": scan_kernels, "achieved": sbytes / (scan_avg / 1e3) / 1e9,
-            "peak": hbm_peak, "unit": "GB/s", "peak_kind": f"{peak_kind} hbm copy",
+    # per-op split of a step, each op graph-replayed alone after an L2 flush
+    n_op = max(5, args.steps // 2)
+    g_scan, g_norm, g_dec = graph_of(torch, scan_call), graph_of(torch, norm_call), \
+        graph_of(torch, decode_call)
+    g_layer = graph_of(torch, layer_prefill)
+    scan_ms = timed_replays(torch, stream, l2, g_scan.replay, n_op)
+    norm_ms = timed_replays(torch, stream, l2, g_norm.replay, n_op)
+    dec_ms = timed_replays(torch, stream, l2, g_dec.replay, n_op)
+    layer_ms = timed_replays(torch, stream, l2, g_layer.replay, n_op)
+    med = lambda v: float(np.median(v))  # noqa: E731
+
+    sbytes = scan_bytes(T, H, P, G, N, nseq, n_init=n_init)
+    scan_avg = sum(scan_ms) / len(scan_ms)
+    scan_kernels = ("scan_pair_kernel + scan_fixup_kernel" if scan_split
+                    else "scan_pair_kernel (two heads of a group per CTA)")
+    roof = {"bound": "hbm", "kernel": scan_kernels,
+            "achieved": sbytes / (scan_avg / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+            "peak_kind": f"{peak_kind} hbm copy",
             "algorithmic_bytes_per_launch": sbytes, "avg_launch_us": scan_avg * 1e3,
-            "traffic": scan_traffic_from_profile(),
-            "traffic_note": "ncu dram read+write per scan call, summed over its kernels "
-                            "(profiles/scan_tc_mamba2_130m.md); the writes stayed in L2",
-            "avg_launch_note": "one scan call (all its kernels) replayed from a graph after "
-                               "an L2 flush"}
+            "traffic": scan_traffic_from_profile("scan_pair_nemotron_h_varlen.md"),
+            "traffic_note": "ncu dram read+write of one scan launch at this workload "
+                            "(profiles/scan_pair_nemotron_h_varlen.md), null if the kernel "
+                            "sources changed since",
+            "avg_launch_note": "one scan call replayed from a graph after an L2 flush, events "
+                               "on the launching stream",
+            "flops_per_launch": T * (G * (KERNEL_CHUNK + 1) * N + H * (KERNEL_CHUNK + 1) * P
+                                     + 4 * H * P * N)}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["tflops"] = roof["flops_per_launch"] / (scan_avg / 1e3) / 1e12
+    roof["frac_of_bf16_peak"] = roof["tflops"] / tc_peak
     nb = norm_bytes(T, d)
+    norm_avg = sum(norm_ms) / len(norm_ms)
+    lb = layer_bytes(T, H, P, G, N, nseq, n_init=n_init, final=True)
+    layer_avg = sum(layer_ms) / len(layer_ms)
 
     extra = {}
     if rank == 0 and not args.no_extra:
-        extra = measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind)
+        extra["mamba2_130m_layer"] = measure_130m(torch, I, ssd, dev, hbm_peak, peak_kind, l2)
+        extra.update(measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind))
 
     # end to end through the public API: every step copies its inputs from pinned host
     # memory and reads its result back.  Copies and compute run on three streams with two
     # sets of device buffers, so the copies of step k+1 and the read-back of step k-1
-    # overlap the compute of step k (the copy engines and the SMs work at once).  A second
-    # host-to-device stream measured no faster: the host link bounds the copies.
+    # overlap the compute of step k (the copy engines and the SMs work at once).
     names = ("x", "dt", "B", "C", "init", "z", "ux", "udt", "uB", "uC")
     host_in = {k: v.detach().cpu().pin_memory() for k, v in
                zip(names, (x, dt, B, C, init, z, ux, udt, uB, uC))}
@@ -372,8 +400,7 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(ev["d2h"])       # step k-2's result was read back
         di, o = st["inp"], st["out"]
         layer_prefill(stream, di, o)
-        ssd.state_update(pool, uidx, di["ux"], di["udt"], A, di["uB"], di["uC"], D=Dp,
-                         dt_bias=bias, y=uy, status=status, stream=stream)
+        decode_call(stream, di)
         ev["comp"].record(stream)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev["comp"])
@@ -410,23 +437,37 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "Mamba2-130M-shaped layer: 2 x 2048 tokens, H=24 P=64 G=1 "
-                               "N=128, chunk 256, scan + gated RMSNorm (d 1536) + decode of "
-                               "both requests", "seqlens": s.seqlens, "H": H, "P": P, "G": G,
-                   "N": N, "chunk_size": s.chunk_size, "tokens_per_step": tokens_per_step,
-                   "l2": L2Flush.DESCRIPTION,
+        "config": {"workload": "Nemotron-H-shaped varlen prefill layer: 4 packed sequences "
+                               "[8192, 3000, 517, 4675] (16384 tokens), H=128 P=64 G=8 N=128, "
+                               "initial states on sequences 0 and 2; scan + D skip + gated "
+                               "RMSNorm (8 groups of 1024) in one call, and the next decode "
+                               "token of the 4 requests on a second stream",
+                   "seqlens": s.seqlens, "H": H, "P": P, "G": G, "N": N,
+                   "chunk_size": s.chunk_size, "kernel_chunk": KERNEL_CHUNK,
+                   "norm_group": group, "prefill_tokens_per_step": tokens_per_step,
+                   "decode_tokens_per_step": nseq, "l2": L2Flush.DESCRIPTION,
                    "launch": "the step's kernels replayed as one CUDA graph: scan + gated norm "
                              "in one call (the norm a programmatic dependent of the scan), the "
                              "decode token on a second stream beside them",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "breakdown_us": {"scan": 1e3 * sum(scan_ms) / len(scan_ms),
-                         "scan_graph_replay": scan_avg * 1e3,
-                         "gated_rmsnorm": 1e3 * sum(norm_ms) / len(norm_ms),
-                         "state_update": 1e3 * sum(upd_ms) / len(upd_ms),
-                         "scan_gated_norm_call": 1e3 * sum(fused_ms) / len(fused_ms)},
+        "breakdown_us": {"scan": 1e3 * med(scan_ms), "gated_rmsnorm": 1e3 * med(norm_ms),
+                         "state_update_4_slots": 1e3 * med(dec_ms),
+                         "scan_gated_norm_call": 1e3 * med(layer_ms),
+                         "note": "each op replayed alone from a graph after an L2 flush"},
         "wall_s_timed_region": t_wall,
         "roofline": roof,
-        "gated_rmsnorm_gbs": nb / (sum(norm_ms) / len(norm_ms) / 1e3) / 1e9,
+        "gated_rmsnorm_nemotron_h": {
+            "workload": "16384 x 8192 bf16, 8 groups of 1024, gated (z), bf16 weight",
+            "avg_launch_us": norm_avg * 1e3, "algorithmic_bytes_per_launch": nb,
+            "achieved_gbs": nb / (norm_avg / 1e3) / 1e9,
+            "frac": nb / (norm_avg / 1e3) / 1e9 / hbm_peak, "peak_kind": f"{peak_kind} hbm copy",
+            "note": "replayed alone from a graph after an L2 flush"},
+        "layer_call_nemotron_h": {
+            "avg_launch_us": layer_avg * 1e3, "algorithmic_bytes_per_launch": lb,
+            "achieved_gbs": lb / (layer_avg / 1e3) / 1e9,
+            "frac": lb / (layer_avg / 1e3) / 1e9 / hbm_peak,
+            "note": "scan + D + gated norm in one call (x, z, out, B, C, dt, states; y not "
+                    "counted)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -437,9 +478,82 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+def measure_130m(torch, I, ssd, dev, hbm_peak, peak_kind, l2, iters=20):
+    """The Mamba2-130M-shaped layer step: 2 x 2048 tokens (H=24, P=64, G=1, N=128, chunk
+    256, initial states), scan + gated norm (d 1536, one group) in one call and one decode
+    token of both requests on a second stream, replayed as one graph after an L2 flush;
+    plus the scan call alone against its roofline."""
+    name = "mamba2_130m"
+    w = I.WORKLOADS[name]
+    s = I.scan_workload(name)
+
+    def T_(t):
+        dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
+        return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
+
+    H, P, G, N, T, nseq = s.H, s.P, s.G, s.N, s.T, s.nseq
+    d = H * P
+    x, dt, A, B, C, Dp, bias, init = (T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D,
+                                                        s.dt_bias, s.initial_states))
+    cu = torch.from_numpy(s.cu_seqlens).to(dev)
+    nrm = I.make_norm_inputs(T, d, w["norm_group"], act="bf16", seed=w["seed"] + 50)
+    z, wt = T_(nrm.z), T_(nrm.weight)
+    y = torch.empty((T, H, P), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((nseq, H, P, N), dtype=torch.float32, device=dev)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    pool = 0.1 * torch.randn((nseq, H, P, N), dtype=torch.float32, device=dev)
+    upd = I.make_update_inputs(nseq, list(range(nseq)), H, P, G, N, act="bf16",
+                               seed=w["seed"] + 60)
+    ux, udt, uB, uC = T_(upd.x), T_(upd.dt), T_(upd.B), T_(upd.C)
+    uidx = torch.arange(nseq, dtype=torch.int32, device=dev)
+    uy = torch.empty((nseq, H, P), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    nws = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu, chunk_size=s.chunk_size)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+
+    def scan_call():
+        ssd.chunk_scan(x, dt, A, B, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=Dp,
+                       dt_bias=bias, initial_states=init, y=y, final_states=fs, workspace=ws)
+
+    def layer():
+        ssd.chunk_scan_gated_norm(x, dt, A, B, C, z, wt, cu_seqlens=cu, chunk_size=s.chunk_size,
+                                  group_size=w["norm_group"], eps=1e-5, D=Dp, dt_bias=bias,
+                                  initial_states=init, out=out, final_states=fs, workspace=ws)
+
+    s_dec = torch.cuda.Stream(device=dev)
+    for _ in range(3):
+        scan_call()
+        layer()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap = torch.cuda.current_stream()
+        s_dec.wait_stream(cap)
+        with torch.cuda.stream(s_dec):
+            ssd.state_update(pool, uidx, ux, udt, A, uB, uC, D=Dp, dt_bias=bias, y=uy)
+        layer()
+        cap.wait_stream(s_dec)
+    step = timed_replays(torch, stream, l2, g.replay, iters)
+    g_scan = graph_of(torch, scan_call)
+    sc = timed_replays(torch, stream, l2, g_scan.replay, iters)
+    st_ms, sc_ms = float(np.median(step)), float(np.median(sc))
+    sb = scan_bytes(T, H, P, G, N, nseq)
+    return {"workload": "Mamba2-130M-shaped layer: 2 x 2048 tokens, H=24 P=64 G=1 N=128, chunk "
+                        "256 (kernel chunk 128), scan + gated RMSNorm (d 1536) in one call + "
+                        "decode of both requests on a second stream",
+            "step_us": st_ms * 1e3, "prefill_tokens_per_s": T / (st_ms / 1e3),
+            "scan_us": sc_ms * 1e3, "scan_split_into_segments": nws > 0,
+            "scan_algorithmic_bytes": sb, "scan_achieved_gbs": sb / (sc_ms / 1e3) / 1e9,
+            "scan_frac_hbm": sb / (sc_ms / 1e3) / 1e9 / hbm_peak,
+            "scan_traffic": scan_traffic_from_profile("scan_tc_mamba2_130m.md"),
+            "peak_kind": f"{peak_kind} hbm copy",
+            "note": "median of graph replays, each after an L2 flush"}
+
+
 def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
-    """Decode at batch 256 on the 512-slot pool, the large varlen prefill scan and one long
-    sequence (split into segments by the library's planner)."""
+    """Decode at batch 256 on the 512-slot pool, the decode layer step, the multi-token
+    update beside the HBM write-only rate, the slot copy, one long sequence on few heads
+    (split into segments by the library's planner), and the Nemotron-H layer path."""
     res = {}
     stream = torch.cuda.current_stream()
     H, P, G, N, S, batch = 128, 64, 8, 128, 512, 256
@@ -510,11 +624,24 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
                                                 inter_states=inter))
     act_m = int((mi >= 0).sum())
     mb = act_m * H * P * N * 4 * (2 + ntok) + bm * ntok * (4 * H * P + 4 * G * N + 4 * H)
+    mb_write = act_m * H * P * N * 4 * (1 + ntok) + bm * ntok * 2 * H * P
+    # the HBM write-only rate on this GPU: a 1 GiB zero fill (torch's fill kernel), the
+    # floor of a write-heavy kernel such as this one (5 of its 6 state passes are writes)
+    wbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    us_w = timed(lambda: wbuf.zero_())
+    write_gbs = (1 << 30) / (us_w / 1e6) / 1e9
+    del wbuf
+    res["hbm_write_floor"] = {
+        "workload": "1 GiB zero fill (write only), back to back", "avg_launch_us": us_w,
+        "achieved_gbs": write_gbs, "frac_of_copy_peak": write_gbs / hbm_peak}
     res["state_update_multi"] = {
         "workload": "4 tokens per request, 64 requests (10% rows -1) on the 512-slot pool, "
                     "state after every token kept", "avg_launch_us": us_m,
         "algorithmic_bytes_per_launch": mb, "achieved_gbs": mb / (us_m / 1e6) / 1e9,
-        "frac": mb / (us_m / 1e6) / 1e9 / hbm_peak, "peak_kind": f"{peak_kind} hbm copy"}
+        "frac": mb / (us_m / 1e6) / 1e9 / hbm_peak, "peak_kind": f"{peak_kind} hbm copy",
+        "written_bytes_per_launch": mb_write,
+        "write_time_at_floor_us": mb_write / (write_gbs * 1e9) * 1e6,
+        "frac_of_write_floor": (mb_write / (write_gbs * 1e9) * 1e6) / us_m}
     # slot copy: 64 states of 4 MiB into a snapshot pool
     snap = torch.empty((64, H, P, N), device=dev)
     ci = torch.from_numpy(I.padded_permutation(S, 64, seed=3300)).to(dev).abs()
@@ -556,15 +683,6 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / iters, nws > 0
 
-    # large varlen prefill
-    s = I.scan_workload("nemotron_h_varlen")
-    us, split = time_scan(s)
-    sb = scan_bytes(s.T, s.H, s.P, s.G, s.N, s.nseq)
-    res["scan_nemotron_h_varlen"] = {
-        "workload": "4 packed sequences [8192,3000,517,4675], H=128 P=64 G=8 N=128, chunk 128 "
-                    "(inputs 0.6 GB > L2)", "tokens_per_s": s.T / (us / 1e6),
-        "avg_launch_us": us, "split_into_segments": split, "algorithmic_bytes_per_launch": sb,
-        "achieved_gbs": sb / (us / 1e6) / 1e9, "frac_hbm": sb / (us / 1e6) / 1e9 / hbm_peak}
     # one long sequence on few heads: the case sequence splitting is for
     s = I.scan_workload("mamba2_130m", seqlens=[16384])
     us, split = time_scan(s)
@@ -577,13 +695,6 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
         "frac_hbm": sb / (us / 1e6) / 1e9 / hbm_peak}
     res.update(measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind))
     return res
-
-
-def layer_bytes(T, H, P, G, N, nseq):
-    """Algorithmic bytes of the prefill layer path (scan, D skip, gated norm) in bf16: x, z
-    and out 2HP each, B and C 2GN each and dt 4H per token, plus the norm weight; y is an
-    intermediate and not counted."""
-    return T * (6 * H * P + 4 * G * N + 4 * H) + 2 * H * P
 
 
 def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
@@ -707,27 +818,53 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
 
 # ----------------------------------------------------------------------------- oracle
 
-def cpu_baseline(s, nrm, w, budget_s=12.0):
-    """The oracle as it stands, on the host cores: the same workload's scan + norm +
-    decode, repeated while under the time budget (at least once)."""
+def oracle_step(s, nrm, upd, group, sl=None):
+    """The oracle (as it stands) on the step's arithmetic, or on the sequences in slice sl
+    of the batch: the scan, the gated norm of the scan's own output, and the decode token
+    of those requests from the scan's final states."""
     import oracle
 
+    cu = np.asarray(s.cu_seqlens)
+    seqs = range(s.nseq) if sl is None else range(s.nseq)[sl]
+    a, b = int(cu[seqs[0]]), int(cu[seqs[-1] + 1])
+    lens = [int(cu[i + 1] - cu[i]) for i in seqs]
+    sub_cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tok = slice(a, b)
+    seq = slice(seqs[0], seqs[-1] + 1)
+    y, fs = oracle.scan_seq(s.x.values[tok], s.dt.values[tok], s.A.values, s.B.values[tok],
+                            s.C.values[tok], D=s.D.values, dt_bias=s.dt_bias.values,
+                            initial_states=s.initial_states.values[seq],
+                            has_initial_state=s.has_initial_state[seq], cu_seqlens=sub_cu)
+    T = b - a
+    oracle.gated_rmsnorm(y.reshape(T, s.H * s.P), nrm.z.values[tok], nrm.weight.values,
+                         group_size=group)
+    oracle.state_update(fs, np.arange(len(lens), dtype=np.int32), upd.x.values[seq],
+                        upd.dt.values[seq], s.A.values, upd.B.values[seq], upd.C.values[seq],
+                        D=s.D.values, dt_bias=s.dt_bias.values)
+    return T
+
+
+def cpu_baseline(s, nrm, w, budget_s=12.0):
+    """The oracle as it stands, on the host cores: the same workload's whole step (scan,
+    the gated norm of its output, the decode token), repeated while under the time budget
+    (at least once)."""
+    from mamba2_ssd_state_gb300 import inputs as I
+
+    upd = I.make_update_inputs(s.nseq, list(range(s.nseq)), s.H, s.P, s.G, s.N, act="bf16",
+                               seed=w["seed"] + 60)
     cores = os.cpu_count()
     t0 = time.perf_counter()
-    reps = 0
+    reps, toks = 0, 0
     while True:
-        oracle.scan_seq(s.x.values, s.dt.values, s.A.values, s.B.values, s.C.values, D=s.D.values,
-                        dt_bias=s.dt_bias.values, initial_states=s.initial_states.values,
-                        cu_seqlens=s.cu_seqlens)
-        oracle.gated_rmsnorm(np.zeros((s.T, s.H * s.P), np.float32), nrm.z.values,
-                             nrm.weight.values, group_size=w["norm_group"])
+        toks += oracle_step(s, nrm, upd, w["norm_group"])
         reps += 1
         if time.perf_counter() - t0 > budget_s or reps >= 500:
             break
     el = time.perf_counter() - t0
-    return {"value": reps * s.T / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} full step(s) of the same workload (scan + norm), "
-                      f"double precision, OpenMP over (sequence, head)",
+    return {"value": toks / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full step(s) of the same workload (scan of the 16384 packed "
+                      f"tokens, gated norm of its output, decode of the 4 requests), double "
+                      f"precision, OpenMP over (sequence, head)",
             "seconds": el}
 
 
@@ -735,39 +872,40 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     from mamba2_ssd_state_gb300 import inputs as I
-    import oracle
     from oracle import build as ob
 
     ob.build()
     w = I.WORKLOADS[WORKLOAD]
     s = I.scan_workload(WORKLOAD)
     nrm = I.make_norm_inputs(s.T, s.H * s.P, w["norm_group"], act="bf16", seed=w["seed"] + 50)
-    # bounded sample per step: one of the two sequences (2048 tokens) through scan + norm
-    L = s.seqlens[0]
-    sl = slice(0, L)
+    upd = I.make_update_inputs(s.nseq, list(range(s.nseq)), s.H, s.P, s.G, s.N, act="bf16",
+                               seed=w["seed"] + 60)
+    # bounded sample per step: sequences 1 and 2 of the batch (3000 + 517 tokens, all 128
+    # heads; sequence 2 with its initial state) through scan, gated norm and decode
+    sl = slice(1, 3)
 
     def step():
-        oracle.scan_seq(s.x.values[sl], s.dt.values[sl], s.A.values, s.B.values[sl],
-                        s.C.values[sl], D=s.D.values, dt_bias=s.dt_bias.values,
-                        initial_states=s.initial_states.values[:1])
-        oracle.gated_rmsnorm(np.zeros((L, s.H * s.P), np.float32), nrm.z.values[sl],
-                             nrm.weight.values, group_size=w["norm_group"])
+        return oracle_step(s, nrm, upd, w["norm_group"], sl)
 
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
+    toks = 0
     for _ in range(args.steps):
-        step()
+        toks += step()
     el = time.perf_counter() - t0
-    v = L * args.steps / el
+    v = toks / el
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "Mamba2-130M-shaped layer (one 2048-token sequence of the "
-                                   "2 x 2048 batch per step), scan + gated RMSNorm"},
+            "config": {"workload": "Nemotron-H-shaped varlen prefill layer (sequences 1 and 2 "
+                                   "of the [8192, 3000, 517, 4675] batch per step: 3517 tokens, "
+                                   "H=128 P=64 G=8 N=128), scan + gated RMSNorm (8 groups of "
+                                   "1024) + decode of those 2 requests"},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
-                             "kind": "oracle", "sample": "one 2048-token sequence per step"},
+                             "kind": "oracle",
+                             "sample": "sequences 1 and 2 (3517 tokens) of the batch per step"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -788,7 +926,8 @@ def profile_only(args):
         return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
 
     if args.profile in ("scan", "scan_large", "scan_split", "norm", "norm_large"):
-        name = WORKLOAD if args.profile in ("scan", "norm", "scan_split") else "nemotron_h_varlen"
+        name = ("mamba2_130m" if args.profile in ("scan", "norm", "scan_split")
+                else "nemotron_h_varlen")
         # scan_split: one 16384-token sequence, which the planner cuts into segments
         s = (I.scan_workload(name, seqlens=[16384]) if args.profile == "scan_split"
              else I.scan_workload(name))

@@ -281,7 +281,9 @@ SSD_API ssd_status ssd_state_update(const ssd_update_args* args, ssd_stream_t st
  * Arguments: as ssd_state_update, with one more leading token axis on the per-token
  * tensors: x [batch, ntok, H, P], dt [batch, ntok, H], B, C [batch, ntok, G, N],
  * y [batch, ntok, H, P] (token t of request b at row b * ntok + t).  inter_states: fp32
- * [batch, ntok, H, P, N], dense, 16-byte aligned, or NULL.  The pool slot receives the
+ * [batch, ntok, H, P, N], dense, 16-byte aligned, or NULL.  B and C must start on a
+ * boundary of four elements (8 bytes in bf16, 16 in fp32; else SSD_ERR_UNSUPPORTED,
+ * nothing launched): they are read four values at a time.  The pool slot receives the
  * state after the last token.  Rows with index -1, out-of-range slots and heads with A
  * not < 0 leave the pool and inter_states untouched and give y = 0 for every token
  * (status bits as ssd_state_update).  ntok >= 1; N in {16, 32, 64, 128}

@@ -218,9 +218,6 @@ cudaError_t launch_state_update_multi(const ssd_update_args& a, int ntok, float*
                                  : launch_multi_t<float>(a, ntok, inter, st);
 }
 
-// Cluster size for a norm group of hpg heads: one head per CTA up to 16 CTAs (a
-// non-portable size above 8), else two heads per CTA if that fits, else the largest
-// portable size that divides hpg.
 // One decode token of a mixer layer after its projections: the state update writes y
 // (into `out` when the caller does not want y: the norm then runs in place, each element
 // read before it is written by the same thread), then the gated norm.  A kernel that

@@ -169,6 +169,9 @@ ssd_status ssd_state_update_multi(const ssd_update_args* args, int32_t ntok,
   if (!decode_n_supported(a.N)) return SSD_ERR_UNSUPPORTED;
   if (a.slot_stride % 4 || ((uintptr_t)a.state_pool & 15u) || ((uintptr_t)inter_states & 15u))
     return SSD_ERR_UNSUPPORTED;
+  // B and C are read four values at a time: rows must start on that boundary
+  const uintptr_t vec = 4u * (a.act_dtype == SSD_BF16 ? 2u : 4u);
+  if (((uintptr_t)a.B % vec) || ((uintptr_t)a.C % vec)) return SSD_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return launch_state_update_multi(a, ntok, inter_states, st) == cudaSuccess ? SSD_OK
                                                                              : SSD_ERR_CUDA;

@@ -175,6 +175,17 @@ def test_decode_ops_reject_bad_arguments(lib):
     a.N = 48
     assert lib.ssd_state_update_multi(ctypes.byref(a), 2, None, None) == 2        # N 48
     a.N = 16
+    # B or C not on a four-element boundary (8 bytes in bf16, 16 in fp32): refused
+    # before anything is launched, since the kernel reads them four values at a time
+    a.act_dtype = ssd.SSD_BF16
+    for field, off in (("B", 2), ("C", 4), ("B", 6)):
+        setattr(a, field, 0x1000 + off)
+        assert lib.ssd_state_update_multi(ctypes.byref(a), 2, None, None) == 2
+        setattr(a, field, 0x1000)
+    a.act_dtype = ssd.SSD_F32
+    a.C = 0x1008                                                                  # 8 of 16
+    assert lib.ssd_state_update_multi(ctypes.byref(a), 2, None, None) == 2
+    a.C = 0x1000
     for gs in (24, 8, 48):   # not a multiple of P, below P, not dividing H*P
         assert lib.ssd_decode_layer_step(ctypes.byref(a), p, p, 0, gs, 1e-5, p, None) == 1
     assert lib.ssd_decode_layer_step(ctypes.byref(a), p, None, 0, 32, 1e-5, p, None) == 1
