@@ -160,3 +160,36 @@ def test_decode_pool_full_size(batch):
                                  dt_bias=u.dt_bias.values[heads], initial_states=st0[None])
         check_bf16(f"pool b={batch} row {b} y", y[b, heads].float().cpu().numpy(), yk[0])
         check_bf16(f"pool b={batch} row {b} slot", pool[slot][heads].cpu().numpy(), fk[0])
+
+
+def test_decode_pool_batch256_every_active_slot():
+    """The batch-256 sweep point compared in full: every active row's y on all 128 heads
+    and every active slot's new [128, 64, 128] state against the oracle; untouched slots
+    bit-identical, -1 rows zero."""
+    H, P, G, N, S, batch = 128, 64, 8, 128, 512, 256
+    idx = I.padded_permutation(S, batch, seed=3000 + batch)
+    u = I.make_update_inputs(1, idx, H, P, G, N, act="bf16", seed=3100 + batch,
+                             pool_values=np.zeros((1, H, P, N), np.float32))
+    gen = torch.Generator(device="cuda").manual_seed(101)
+    pool = torch.randn((S, H, P, N), generator=gen, device="cuda", dtype=torch.float32)
+    active = np.array([int(v) for v in idx if v >= 0])
+    act_t = torch.from_numpy(active).long().cuda()
+    before_active = pool[act_t].cpu().numpy()
+    before = pool.clone()
+    y, bits = _update_gpu(u, pool)
+    torch.cuda.synchronize()
+    assert bits == 0
+    untouched = torch.ones(S, dtype=torch.bool, device="cuda")
+    untouched[act_t] = False
+    assert torch.equal(pool[untouched], before[untouched])
+    del before
+    # the oracle on a pool of the active slots only, rows re-indexed into it
+    pos = {int(s): k for k, s in enumerate(active)}
+    idx_o = np.array([pos.get(int(v), -1) for v in idx], dtype=np.int32)
+    new_o, y_o, st = oracle.state_update(before_active, idx_o, u.x.values, u.dt.values,
+                                         u.A.values, u.B.values, u.C.values, D=u.D.values,
+                                         dt_bias=u.dt_bias.values)
+    assert st == 0
+    check_bf16("pool b=256 all rows y", y.float().cpu().numpy(), y_o)
+    assert np.all(y_o[idx == -1] == 0)
+    check_bf16("pool b=256 all active slots", pool[act_t].cpu().numpy(), new_o)
