@@ -257,15 +257,26 @@ def run_ours(args, rank, world, local_rank):
         ssd.state_update(pool, uidx, i["ux"], i["udt"], A, i["uB"], i["uC"], D=Dp, dt_bias=bias,
                          y=uy, status=status, stream=st)
 
+    # the call's workspace: the ready queue of its overlapped form (the norm normalises the
+    # scan's finished chunks while the scan runs), or a split's, or none
+    lws_bytes = ssd.chunk_scan_gated_norm_workspace_size(x, B, C, z, wt, out, cu_seqlens=cu,
+                                                         chunk_size=s.chunk_size,
+                                                         group_size=group)
+    lws = torch.empty(max(lws_bytes, 1), dtype=torch.uint8, device=dev)
+    scan_split_bytes = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu,
+                                                     chunk_size=s.chunk_size)
+    norm_form = ("chained" if lws_bytes == 0 or lws_bytes == scan_split_bytes
+                 else "overlapped")
+
     def layer_prefill(st=None, inp=None, out_=None):
-        """The prefill half of the layer in one call: scan, then the gated norm launched as
-        its programmatic dependent, normalising in place in out."""
+        """The prefill half of the layer in one call: scan, D skip and gated norm, the norm
+        a programmatic dependent of the scan that normalises in place in out."""
         i = inp or dict(x=x, dt=dt, B=B, C=C, init=init, z=z)
         ssd.chunk_scan_gated_norm(i["x"], i["dt"], A, i["B"], i["C"], i["z"], wt, cu_seqlens=cu,
                                   chunk_size=s.chunk_size, group_size=group, eps=1e-5, D=Dp,
                                   dt_bias=bias, initial_states=i["init"], has_initial_state=hi,
                                   out=out if out_ is None else out_, final_states=fs,
-                                  status=status, stream=st)
+                                  status=status, stream=st, workspace=lws)
 
     # the scan is one launch, or two when the library splits the sequences into segments
     scan_split = ssd.chunk_scan_workspace_size(x, B, C, cu_seqlens=cu,
@@ -449,6 +460,10 @@ def run_ours(args, rank, world, local_rank):
                    "launch": "the step's kernels replayed as one CUDA graph: scan + gated norm "
                              "in one call (the norm a programmatic dependent of the scan), the "
                              "decode token on a second stream beside them",
+                   "norm_form": norm_form + (
+                       ": the scan appends each finished 128-token chunk of each norm group "
+                       "to a queue and the norm kernel normalises those rows while the scan "
+                       "runs" if norm_form == "overlapped" else ": the norm follows the scan"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "breakdown_us": {"scan": 1e3 * med(scan_ms), "gated_rmsnorm": 1e3 * med(norm_ms),
                          "state_update_4_slots": 1e3 * med(dec_ms),

@@ -206,26 +206,49 @@ SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_strea
  * gated_rmsnorm over its output (the layer order scan, D skip, gated RMSNorm of the
  * Nemotron-H layer path; vt::RmsNormGatedGroup of [vllm.cpp #566]), in one call.
  *
- * The two run as kernels back to back on the stream; the norm is launched as a
- * programmatic dependent of the scan.  Its blocks take the SMs the scan leaves idle
- * and load z and the weights while the scan runs, then wait for the scan to complete
- * (griddepcontrol.wait) before they read y, which is still in L2.  The tensor-core scan
- * kernels signal their dependents early (griddepcontrol.launch_dependents): a kernel a
- * caller launches after ssd_chunk_scan with programmatic stream serialisation must
- * likewise wait (cudaGridDependencySynchronize) before it reads the scan's outputs.
+ * Two forms, the same results bit for bit:
+ *   - overlapped: when the scan runs two heads per CTA unsplit (bf16, group_size a
+ *     multiple of 64, 16-byte aligned rows) and args->workspace holds at least
+ *     ssd_chunk_scan_gated_norm_workspace_size bytes (256-byte aligned; the call zeroes
+ *     the bytes it uses, with a memset on the stream), the scan appends every finished
+ *     128-token chunk of every norm group to a queue in the workspace, and the norm,
+ *     launched as a programmatic dependent of the scan, normalises those rows while the
+ *     scan works on later chunks.  Each wait of the norm on the queue is bounded (about
+ *     2 s; SSD_DEV_TIMEOUT in d_status when one gives up, as when the scan aborts).
+ *   - chained: otherwise the norm follows the scan, also as a programmatic dependent: its
+ *     blocks take the SMs the scan leaves idle and load z and the weights while the scan
+ *     runs, then wait for the scan to complete (griddepcontrol.wait) before they read y.
+ * The tensor-core scan kernels signal their dependents early
+ * (griddepcontrol.launch_dependents): a kernel a caller launches after ssd_chunk_scan
+ * with programmatic stream serialisation must likewise wait
+ * (cudaGridDependencySynchronize) before it reads the scan's outputs.
  *
  * Arguments: args as ssd_chunk_scan, except that args->y may be NULL (then y is written
- * into out and normalised in place); z [T, H*P] act_dtype or NULL (no gate), which must
- * share no byte with y or out (else SSD_ERR_INVALID_ARG) and must not be written by the
- * scan; norm_weight [H*P] weight_dtype; out [T, H*P] act_dtype, may be args->y.
- * group_size: channels per norm group, dividing H*P.  eps >= 0.  Errors are those of
- * ssd_chunk_scan and gated_rmsnorm, all returned before any launch.  With T == 0 only
- * the final states are written.
+ * into out and normalised in place) and that the workspace also serves the overlapped
+ * form; z [T, H*P] act_dtype or NULL (no gate), which must share no byte with y or out
+ * (else SSD_ERR_INVALID_ARG) and must not be written by the scan; norm_weight [H*P]
+ * weight_dtype; out [T, H*P] act_dtype, may be args->y.  group_size: channels per norm
+ * group, dividing H*P.  eps >= 0.  Errors are those of ssd_chunk_scan and gated_rmsnorm,
+ * all returned before any launch.  With T == 0 only the final states are written.
  * ------------------------------------------------------------------------------------ */
 SSD_API ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const void* z,
                                              const void* norm_weight, ssd_dtype weight_dtype,
                                              int32_t group_size, float eps, void* out,
                                              ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * ssd_chunk_scan_gated_norm_workspace_size -- device workspace (bytes) that
+ * ssd_chunk_scan_gated_norm wants for these arguments: the split of the scan when its
+ * planner would split (ssd_chunk_scan_workspace_size), else the ready queue of the
+ * overlapped form (about 12 bytes per 128-token chunk and norm group), else 0.  Reads
+ * only shapes, pointers' alignment and the plan inputs of args (no device memory);
+ * invalid arguments give 0.  The library does not name a counterpart of this split of
+ * the scan + norm call in the source pages: it exists so that the norm may run while the
+ * scan does.
+ * ------------------------------------------------------------------------------------ */
+SSD_API size_t ssd_chunk_scan_gated_norm_workspace_size(const ssd_scan_args* args,
+                                                        const void* z, const void* norm_weight,
+                                                        int32_t group_size, const void* out);
 
 /* ------------------------------------------------------------------------------------
  * ssd_state_update -- one decode token per request on a pooled state cache,

@@ -81,28 +81,24 @@ template <> struct Vec8<float> {
 // covers 32 consecutive vectors (coalesced), and at most 4 vectors per thread keep the
 // register count low enough for several blocks per SM.  Warp partial sums meet in
 // shared memory when a group spans several warps.
-template <typename TA, typename TW, int VPT, int TPG>
-__global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
-                                                       const TA* __restrict__ z,
-                                                       const TW* __restrict__ w, TA* out,
-                                                       int64_t units, int d, int gs, float eps) {
-  constexpr int GPB = 256 / TPG;  // groups per block
-  __shared__ float part[8];
+// One (row, group) unit: the threads of a 256-thread block with the same threadIdx / TPG
+// work on it; every thread of the block calls this (valid or not), since groups of more
+// than a warp meet at block barriers.  pdl: wait for the kernel before (the producer of
+// x) after loading z.
+template <typename TA, typename TW, int VPT, int TPG, bool kPdl>
+__device__ __forceinline__ void norm_unit(const TA* x, const TA* __restrict__ z,
+                                          const TW* __restrict__ w, TA* out, bool valid,
+                                          size_t base, int col0, int gs, float eps,
+                                          float* part) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tig = threadIdx.x % TPG;
-  const int64_t unit = (int64_t)blockIdx.x * GPB + threadIdx.x / TPG;
-  const bool valid = unit < units;
-  const int ngroups = d / gs;
-  const int64_t row = valid ? unit / ngroups : 0;
-  const int col0 = valid ? (int)(unit % ngroups) * gs : 0;
-  const size_t base = (size_t)row * d + col0;
   float g[VPT][8];
   float ss = 0.f;
   if (valid && z) {  // z first: it may be read before the producer of x has finished
 #pragma unroll
     for (int i = 0; i < VPT; ++i) Vec8<TA>::load(z + base + 8 * (tig + TPG * i), g[i]);
   }
-  tc::griddep_wait();
+  if constexpr (kPdl) tc::griddep_wait();
   if (valid) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -125,6 +121,7 @@ __global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
     ss = 0.f;
 #pragma unroll
     for (int k = 0; k < WPG; ++k) ss += part[w0 + k];
+    __syncthreads();  // part is rewritten by the next unit
   }
   if (!valid) return;
   const float r = rsqrtf(ss / (float)gs + eps);
@@ -137,6 +134,97 @@ __global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
     for (int e = 0; e < 8; ++e) o[e] = g[i][e] * r * wv[e];
     Vec8<TA>::store(out + base + off, o);
   }
+}
+
+template <typename TA, typename TW, int VPT, int TPG>
+__global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
+                                                       const TA* __restrict__ z,
+                                                       const TW* __restrict__ w, TA* out,
+                                                       int64_t units, int d, int gs, float eps) {
+  constexpr int GPB = 256 / TPG;  // groups per block
+  __shared__ float part[8];
+  const int64_t unit = (int64_t)blockIdx.x * GPB + threadIdx.x / TPG;
+  const bool valid = unit < units;
+  const int ngroups = d / gs;
+  const int64_t row = valid ? unit / ngroups : 0;
+  const int col0 = valid ? (int)(unit % ngroups) * gs : 0;
+  norm_unit<TA, TW, VPT, TPG, true>(x, z, w, out, valid, (size_t)row * d + col0, col0, gs, eps,
+                                    part);
+}
+
+// The norm of the scan + norm call, fed by the scan's ready queue: each block takes the
+// next queue slot, waits (bounded) until the scan has appended a task there, and
+// normalises that task's rows of one group with the per-unit arithmetic of
+// norm_vec_kernel, so its outputs are bit for bit those of the standalone norm.  The
+// blocks start once every scan CTA has started (programmatic dependent launch), on SMs
+// the scan leaves free, and never wait for the scan grid itself.
+template <typename TA, typename TW, int VPT, int TPG>
+__global__ void __launch_bounds__(256) norm_ready_kernel(const TA* x,
+                                                         const TA* __restrict__ z,
+                                                         const TW* __restrict__ w, TA* out,
+                                                         const int32_t* __restrict__ cu,
+                                                         int nseq, int T, int d, int gs,
+                                                         float eps, ReadyQueue rq,
+                                                         uint32_t* status) {
+  constexpr int GPB = 256 / TPG;  // rows per block step
+  constexpr int kRows = 128 / kReadyParts;
+  __shared__ float part[8];
+  __shared__ long long red[8];
+  __shared__ unsigned long long task;
+  // the queue's length: every chunk of every sequence the scan accepts, once per group
+  long long mine = 0;
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int t0 = cu[s], t1 = cu[s + 1];
+    if (0 <= t0 && t0 <= t1 && t1 <= T) mine += (t1 - t0 + 127) / 128;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mine;
+  __syncthreads();
+  long long total = 0;
+  for (int k = 0; k < 8; ++k) total += red[k];
+  total *= (long long)rq.ngroups * kReadyParts;
+  for (;;) {
+    if (threadIdx.x == 0) {
+      unsigned long long v = 0;
+      const long long idx = atomicAdd(rq.head, 1);
+      if (idx < total) {
+        const volatile unsigned long long* slot = rq.q + idx;
+        const long long t_start = clock64();
+        while ((v = *slot) == 0ull) {
+          if (*(volatile int*)rq.abort) break;
+          if (clock64() - t_start > SSD_WAIT_LIMIT_CYCLES) {
+            atomicExch(rq.abort, 1);
+            set_status(status, SSD_DEV_TIMEOUT);
+            break;
+          }
+          __nanosleep(128);
+        }
+        __threadfence();  // the task's rows of y are visible from here on
+      }
+      task = v;
+    }
+    __syncthreads();
+    const unsigned long long v = task;
+    __syncthreads();
+    if (v == 0ull) break;
+    const int s = (int)(v >> 32) - 1;
+    const int c = (int)((v >> 15) & 0x1ffffu);
+    const int k = (int)((v >> 12) & 7u);
+    const int grp = (int)(v & 0xfffu);
+    const int t1 = cu[s + 1];
+    const int r0 = cu[s] + 128 * c + kRows * k;
+    const int r1 = min(t1, r0 + kRows);
+    const int col0 = grp * gs;
+    for (int rb = r0; rb < r1; rb += GPB) {  // the same trip count in every thread
+      const int row = rb + threadIdx.x / TPG;
+      norm_unit<TA, TW, VPT, TPG, false>(x, z, w, out, row < r1, (size_t)row * d + col0, col0,
+                                         gs, eps, part);
+    }
+  }
+  // end no earlier than the scan grid, so that work after this call on the stream finds
+  // the scan's final states written too
+  tc::griddep_wait();
 }
 
 // Any group size: one warp per (row, group), two passes (the second re-reads x and z,
@@ -172,6 +260,8 @@ __global__ void __launch_bounds__(256) norm_generic_kernel(const TA* x,
 
 // 256-thread blocks on `st`; with pdl the launch may begin before the previous kernel on
 // the stream has completed (programmatic stream serialisation).
+constexpr int kReadyBlocksPerSm = 4;  // resident ready-queue norm blocks per free SM
+
 template <typename... P, typename... A>
 cudaError_t launch256(void (*kernel)(P...), int64_t blocks, bool pdl, cudaStream_t st,
                       A... args) {
@@ -187,6 +277,26 @@ cudaError_t launch256(void (*kernel)(P...), int64_t blocks, bool pdl, cudaStream
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Vector path: the smallest group of threads (32..256) with at most 4 vectors each, for
+// 16-byte aligned rows; false (generic path) otherwise.
+bool vec_shape(const void* x, const void* z, const void* w, const void* out, int d, int gs,
+               size_t act_bytes, int* tpg, int* vpt) {
+  *tpg = *vpt = 0;
+  const bool aligned = ((uintptr_t)x % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
+                       (z == nullptr || (uintptr_t)z % 16 == 0) && ((uintptr_t)w % 16 == 0) &&
+                       ((size_t)d * act_bytes) % 16 == 0;
+  if (!aligned || gs % 8 != 0) return false;
+  for (int t = 32; t <= 256; t *= 2) {
+    const int nvec = gs / 8;
+    if (nvec % t == 0 && nvec / t <= 4) {
+      *tpg = t;
+      *vpt = nvec / t;
+      return true;
+    }
+  }
+  return false;
+}
+
 template <typename TA, typename TW>
 cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out, int64_t rows,
                          int d, int gs, float eps, bool pdl, cudaStream_t st) {
@@ -196,21 +306,8 @@ cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out,
   const TA* zp = static_cast<const TA*>(z);
   const TW* wp = static_cast<const TW*>(w);
   TA* op = static_cast<TA*>(out);
-  const bool aligned = ((uintptr_t)x % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
-                       (z == nullptr || (uintptr_t)z % 16 == 0) && ((uintptr_t)w % 16 == 0) &&
-                       ((size_t)d * sizeof(TA)) % 16 == 0;
-  // vector path: the smallest group of threads (32..256) with at most 4 vectors each
-  int tpg = 0, vpt = 0;
-  if (aligned && gs % 8 == 0) {
-    for (int t = 32; t <= 256; t *= 2) {
-      const int nvec = gs / 8;
-      if (nvec % t == 0 && nvec / t <= 4) {
-        tpg = t;
-        vpt = nvec / t;
-        break;
-      }
-    }
-  }
+  int tpg, vpt;
+  vec_shape(x, z, w, out, d, gs, sizeof(TA), &tpg, &vpt);
   const int gpb = tpg ? 256 / tpg : 8;
   const int64_t vblocks = (units + gpb - 1) / gpb;
 #define SSD_NORM_CASE(V, T)                                                                 \
@@ -225,7 +322,84 @@ cudaError_t launch_typed(const void* x, const void* z, const void* w, void* out,
                    eps);
 }
 
+// The ready-queue norm: a persistent grid of a few blocks per SM.
+template <typename TA, typename TW>
+cudaError_t launch_ready_typed(const void* x, const void* z, const void* w, void* out,
+                               const int32_t* cu, int nseq, int T, int d, int gs, float eps,
+                               const ReadyQueue& rq, uint32_t* status, cudaStream_t st) {
+  int tpg, vpt;
+  if (!vec_shape(x, z, w, out, d, gs, sizeof(TA), &tpg, &vpt)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const int64_t blocks = (int64_t)kReadyBlocksPerSm * sms;
+  const TA* xp = static_cast<const TA*>(x);
+  const TA* zp = static_cast<const TA*>(z);
+  const TW* wp = static_cast<const TW*>(w);
+  TA* op = static_cast<TA*>(out);
+#define SSD_READY_CASE(V, TP)                                                                \
+  if (vpt == V && tpg == TP)                                                                  \
+    return launch256(norm_ready_kernel<TA, TW, V, TP>, blocks, true, st, xp, zp, wp, op, cu,   \
+                     nseq, T, d, gs, eps, rq, status);
+  SSD_READY_CASE(1, 32) SSD_READY_CASE(2, 32) SSD_READY_CASE(3, 32) SSD_READY_CASE(4, 32)
+  SSD_READY_CASE(3, 64) SSD_READY_CASE(4, 64) SSD_READY_CASE(3, 128) SSD_READY_CASE(4, 128)
+  SSD_READY_CASE(3, 256) SSD_READY_CASE(4, 256)
+#undef SSD_READY_CASE
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+bool norm_ready_supported(const void* x, const void* z, const void* w, const void* out, int d,
+                          int gs, ssd_dtype act) {
+  int tpg, vpt;
+  return vec_shape(x, z, w, out, d, gs, act == SSD_BF16 ? 2 : 4, &tpg, &vpt);
+}
+
+cudaError_t launch_norm_ready(const void* x, const void* z, const void* w, void* out,
+                              const int32_t* cu, int nseq, int T, int d, int gs, float eps,
+                              ssd_dtype act, ssd_dtype wt, const ReadyQueue& rq,
+                              uint32_t* status, cudaStream_t st) {
+  using bf = __nv_bfloat16;
+  if (act == SSD_BF16)
+    return wt == SSD_BF16
+               ? launch_ready_typed<bf, bf>(x, z, w, out, cu, nseq, T, d, gs, eps, rq, status, st)
+               : launch_ready_typed<bf, float>(x, z, w, out, cu, nseq, T, d, gs, eps, rq, status,
+                                               st);
+  return wt == SSD_BF16
+             ? launch_ready_typed<float, bf>(x, z, w, out, cu, nseq, T, d, gs, eps, rq, status, st)
+             : launch_ready_typed<float, float>(x, z, w, out, cu, nseq, T, d, gs, eps, rq, status,
+                                                st);
+}
+
+size_t ready_queue_bytes(int64_t T, int nseq, int ngroups) {
+  const int64_t nid = (T + 127) / 128 + nseq;
+  const size_t ntask = (size_t)nid * ngroups;
+  const size_t bytes = ntask * sizeof(int) + ntask * kReadyParts * sizeof(unsigned long long) +
+                       4 * sizeof(int);
+  return (bytes + 255) / 256 * 256;
+}
+
+ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs) {
+  const int64_t nid = (T + 127) / 128 + nseq;
+  const size_t ntask = (size_t)nid * ngroups;
+  char* p = static_cast<char*>(ws);
+  ReadyQueue rq;
+  // the 8-byte task slots first (the workspace is 256-byte aligned), then the counters
+  rq.q = reinterpret_cast<unsigned long long*>(p);
+  p += ntask * kReadyParts * sizeof(unsigned long long);
+  rq.cnt = reinterpret_cast<int*>(p);
+  p += ntask * sizeof(int);
+  rq.head = reinterpret_cast<int*>(p);
+  rq.tail = rq.head + 1;
+  rq.abort = rq.head + 2;
+  rq.nid = nid;
+  rq.ngroups = ngroups;
+  rq.gs = gs;
+  rq.target = 4 * (gs / 64);
+  return rq;
+}
 
 cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, void* out,
                                  int64_t rows, int d, int gs, float eps, ssd_dtype act,

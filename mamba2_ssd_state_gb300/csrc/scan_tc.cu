@@ -78,9 +78,6 @@ constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
 constexpr int kThreads = 32 * (kDecayWarp + 1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFactorLimit = 64.f;            // log2 bound of a factorised decay factor
-#ifndef SSD_WAIT_LIMIT_CYCLES
-#define SSD_WAIT_LIMIT_CYCLES 4000000000LL  // about 2 s
-#endif
 constexpr long long kWaitLimit = SSD_WAIT_LIMIT_CYCLES;  // SM cycles a wait may take
 
 #ifdef SSD_FAULT_INJECT
@@ -113,6 +110,7 @@ struct TcParams {
   float* ws_h;    // split sequences: local end state per segment [nseg, H, P, N]
   float* ws_cs;   // split sequences: log2 decay from the segment start to each token [T, H]
   int nseq, T, H, P, G, npb, dt_softplus, segc;
+  ReadyQueue rq;  // unsplit two-head scan of the scan + norm call: finished rows; cnt NULL = off
 };
 
 template <int PB>
@@ -1315,7 +1313,8 @@ bool opt_in(K kernel, int bytes, std::atomic<bool>* done) {
 }
 
 template <int PB>
-ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t st) {
+ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t st,
+                     const ReadyQueue* rq = nullptr) {
   using L = Layout<PB>;
   const bool pair = plan.hb == 2;
   const int64_t xs = a.x_stride_t ? a.x_stride_t : (int64_t)a.H * a.P;
@@ -1334,10 +1333,13 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
     return SSD_ERR_CUDA;
   // dynamic shared memory above 48 KB is opted into once per kernel and device
   static std::atomic<bool> set_one[kMaxDevices], set_one_split[kMaxDevices],
-      set_pair[kMaxDevices], set_pair_split[kMaxDevices], set_fix[kMaxDevices];
+      set_pair[kMaxDevices], set_pair_split[kMaxDevices], set_pair_ready[kMaxDevices],
+      set_fix[kMaxDevices];
   const bool split = plan.segc > 0;
   bool ok;
-  if (pair)
+  if (pair && rq)
+    ok = opt_in(scan_pair_kernel<false, true>, pair::kSmemBytes, set_pair_ready);
+  else if (pair)
     ok = split ? opt_in(scan_pair_kernel<true>, pair::kSmemBytes, set_pair_split)
                : opt_in(scan_pair_kernel<false>, pair::kSmemBytes, set_pair);
   else
@@ -1368,8 +1370,15 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   prm.npb = a.P / PB;
   prm.dt_softplus = a.dt_softplus;
   prm.segc = plan.segc;
+  prm.rq = ReadyQueue{};
+  if (rq) {
+    if (!pair || split) return SSD_ERR_UNSUPPORTED;
+    prm.rq = *rq;
+  }
   const long long grid = plan.nseg * (a.H / plan.hb) * prm.npb;
-  if (pair) {
+  if (pair && rq) {
+    scan_pair_kernel<false, true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
+  } else if (pair) {
     if (split)
       scan_pair_kernel<true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
     else
@@ -1440,26 +1449,57 @@ size_t scan_tc_workspace_size(const ssd_scan_args& a, size_t ws_limit) {
   return plan.ws_bytes;
 }
 
-ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t st, size_t ws_limit) {
-  ScanPlan plan;
-  if (!plan_scan(a, a.seg_chunks >= 0, &plan, ws_limit)) {
+namespace {
+// The plan a call runs: the cheapest (splits within ws_limit when allowed), run unsplit
+// when the caller's workspace is too small for the split it chose.
+ssd_status final_plan(const ssd_scan_args& a, size_t ws_limit, ScanPlan* plan) {
+  if (!plan_scan(a, a.seg_chunks >= 0, plan, ws_limit)) {
     if (a.seg_chunks >= 1) return SSD_ERR_UNSUPPORTED;
-    if (!plan_scan(a, false, &plan)) return SSD_ERR_UNSUPPORTED;
+    if (!plan_scan(a, false, plan)) return SSD_ERR_UNSUPPORTED;
   }
-  if (plan.segc > 0) {
+  if (plan->segc > 0) {
     const bool ws_ok = a.workspace && ((uintptr_t)a.workspace & 255u) == 0 &&
-                       a.workspace_bytes >= plan.ws_bytes;
+                       a.workspace_bytes >= plan->ws_bytes;
     if (!ws_ok) {
       if (a.seg_chunks >= 1) return SSD_ERR_INVALID_ARG;
-      if (!plan_scan(a, false, &plan)) return SSD_ERR_UNSUPPORTED;  // run unsplit
+      if (!plan_scan(a, false, plan)) return SSD_ERR_UNSUPPORTED;  // run unsplit
     }
   }
+  return SSD_OK;
+}
+}  // namespace
+
+ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t st, size_t ws_limit) {
+  ScanPlan plan;
+  const ssd_status v = final_plan(a, ws_limit, &plan);
+  if (v != SSD_OK) return v;
   switch (plan.pb) {
     case 64: return launch_pb<64>(a, plan, st);
     case 32: return launch_pb<32>(a, plan, st);
     case 16: return launch_pb<16>(a, plan, st);
   }
   return SSD_ERR_UNSUPPORTED;
+}
+
+// The norm kernel of the overlapped form starts only once every scan CTA has started, so
+// the form pays only when the scan grid takes at most two waves (one CTA per SM): then
+// the norm runs beside the scan's last wave.  Deeper grids leave it no time to overlap.
+constexpr int kReadyMaxWaves = 2;
+
+bool scan_tc_ready_plan(const ssd_scan_args& a) {
+  if (!scan_tc_supported(a)) return false;
+  ScanPlan plan;
+  if (final_plan(a, SIZE_MAX, &plan) != SSD_OK || plan.hb != 2 || plan.segc != 0) return false;
+  const long long grid = (long long)a.nseq * (a.H / 2) * (a.P / 64);
+  return grid <= (long long)kReadyMaxWaves * sm_count();
+}
+
+ssd_status launch_scan_tc_ready(const ssd_scan_args& a, const ReadyQueue& rq, cudaStream_t st) {
+  ScanPlan plan;
+  const ssd_status v = final_plan(a, SIZE_MAX, &plan);
+  if (v != SSD_OK) return v;
+  if (plan.hb != 2 || plan.segc != 0) return SSD_ERR_UNSUPPORTED;
+  return launch_pb<64>(a, plan, st, &rq);
 }
 
 }  // namespace ssd

@@ -49,6 +49,19 @@ ssd_status validate_update(const ssd_update_args* a) {
   return SSD_OK;
 }
 
+// Workspace of the overlapped scan + norm (0 = the call runs the norm after the scan):
+// the two-head scan unsplit, bf16, a norm group of whole 64-channel head blocks, and a
+// norm kernel for this group size and alignment.
+size_t gated_norm_ready_bytes(const ssd_scan_args& a, const void* z, const void* w,
+                              int32_t group_size, const void* out) {
+  const int64_t d = (int64_t)a.H * a.P;
+  if (a.impl == SSD_IMPL_SIMT || a.act_dtype != SSD_BF16 || group_size % 64 != 0) return 0;
+  if (d / group_size >= kReadyMaxGroups || a.T > kReadyMaxChunks * 128) return 0;
+  if (!norm_ready_supported(a.y, z, w, out, (int)d, group_size, a.act_dtype)) return 0;
+  if (!scan_tc_ready_plan(a)) return 0;
+  return ready_queue_bytes(a.T, a.nseq, (int)(d / group_size));
+}
+
 }  // namespace
 
 extern "C" {
@@ -114,13 +127,45 @@ ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const void* z,
     return u < w + bytes && w < u + bytes;
   };
   if (z && (overlap(z, a.y) || overlap(z, out))) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the overlapped form: the norm consumes the scan's finished chunks while it runs
+  const size_t need = gated_norm_ready_bytes(a, z, norm_weight, group_size, out);
+  if (need > 0 && a.workspace && ((uintptr_t)a.workspace & 255u) == 0 &&
+      a.workspace_bytes >= need) {
+    const int ngroups = (int)(d / group_size);
+    if (cudaMemsetAsync(a.workspace, 0, need, st) != cudaSuccess) return SSD_ERR_CUDA;
+    const ReadyQueue rq = ready_queue_at(a.workspace, a.T, a.nseq, ngroups, group_size);
+    v = launch_scan_tc_ready(a, rq, st);
+    if (v != SSD_OK) return v;
+    return launch_norm_ready(a.y, z, norm_weight, out, a.cu_seqlens, a.nseq, a.T, (int)d,
+                             group_size, eps, a.act_dtype, weight_dtype, rq, a.d_status,
+                             st) == cudaSuccess
+               ? SSD_OK
+               : SSD_ERR_CUDA;
+  }
   v = ssd_chunk_scan(&a, stream);
   if (v != SSD_OK) return v;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return launch_gated_rmsnorm(a.y, z, norm_weight, out, a.T, (int)d, group_size, eps,
                               a.act_dtype, weight_dtype, st, /*pdl=*/true) == cudaSuccess
              ? SSD_OK
              : SSD_ERR_CUDA;
+}
+
+size_t ssd_chunk_scan_gated_norm_workspace_size(const ssd_scan_args* args, const void* z,
+                                                const void* norm_weight, int32_t group_size,
+                                                const void* out) {
+  if (!args || args->struct_size < sizeof(ssd_scan_args)) return 0;
+  ssd_scan_args a = *args;
+  if (!a.y) a.y = const_cast<void*>(out);  // only its address is looked at
+  if (validate_scan(&a) != SSD_OK || a.T == 0 || !norm_weight || !out) return 0;
+  const int64_t d = (int64_t)a.H * a.P;
+  if (group_size < 1 || d % group_size != 0) return 0;
+  // a split the scan would choose takes the workspace (the norm then follows the scan)
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  const size_t split = a.impl == SSD_IMPL_SIMT ? 0 : scan_tc_workspace_size(a);
+  if (split > 0) return split;
+  return gated_norm_ready_bytes(a, z, norm_weight, group_size, out);
 }
 
 size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args) {

@@ -75,6 +75,9 @@ def load_library(path: str | None = None):
         lib.ssd_chunk_scan_gated_norm.argtypes = [ctypes.POINTER(ScanArgs), _vp, _vp,
                                                   ctypes.c_int, _i32, ctypes.c_float, _vp, _vp]
         lib.ssd_chunk_scan_gated_norm.restype = ctypes.c_int
+        lib.ssd_chunk_scan_gated_norm_workspace_size.argtypes = [ctypes.POINTER(ScanArgs), _vp,
+                                                                 _vp, _i32, _vp]
+        lib.ssd_chunk_scan_gated_norm_workspace_size.restype = ctypes.c_size_t
         lib.ssd_state_update_multi.argtypes = [ctypes.POINTER(UpdateArgs), _i32, _vp, _vp]
         lib.ssd_state_update_multi.restype = ctypes.c_int
         lib.ssd_decode_layer_step.argtypes = [ctypes.POINTER(UpdateArgs), _vp, _vp, ctypes.c_int,
@@ -203,7 +206,15 @@ def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_s
     a, y, final_states, _ws = _scan_args(
         lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus, initial_states,
         has_initial_state, y if y is not None else out.view(T, H, P), final_states,
-        return_final_states, status, impl, p_block, seg_chunks, workspace, head_block)
+        return_final_states, status, impl, p_block, seg_chunks, workspace, head_block,
+        alloc_ws=False)
+    if workspace is None:
+        # the split of the scan, or the ready queue of the overlapped form
+        nbytes = lib.ssd_chunk_scan_gated_norm_workspace_size(
+            ctypes.byref(a), _ptr(z), _ptr(norm_weight), int(group_size), _ptr(out))
+        if nbytes:
+            _ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            a.workspace, a.workspace_bytes = _ptr(_ws), _ws.numel()
     _raise(lib.ssd_chunk_scan_gated_norm(ctypes.byref(a), _ptr(z), _ptr(norm_weight),
                                          _act(norm_weight), int(group_size), float(eps),
                                          _ptr(out), _stream(stream)),
@@ -213,7 +224,7 @@ def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_s
 
 def _scan_args(lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softplus,
                initial_states, has_initial_state, y, final_states, return_final_states, status,
-               impl, p_block, seg_chunks, workspace, head_block=0):
+               impl, p_block, seg_chunks, workspace, head_block=0, alloc_ws=True):
     """ssd_scan_args for one scan call, with the outputs (and a workspace from torch's
     allocator, when the plan wants one and none was passed) made where missing."""
     T, H, P = x.shape
@@ -258,7 +269,7 @@ def _scan_args(lib, x, dt, A, B, C, cu_seqlens, chunk_size, D, dt_bias, dt_softp
     a.y, a.final_states, a.d_status = _ptr(y), _ptr(final_states), _ptr(status)
     a.impl, a.p_block = IMPL[impl], int(p_block)
     a.seg_chunks, a.head_block = int(seg_chunks), int(head_block)
-    if workspace is None and a.seg_chunks >= 0:
+    if workspace is None and a.seg_chunks >= 0 and alloc_ws:
         nbytes = lib.ssd_chunk_scan_workspace_size(ctypes.byref(a))
         if nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -287,6 +298,31 @@ def chunk_scan_workspace_size(x, B, C, *, cu_seqlens, chunk_size, impl="auto", p
     a.impl, a.p_block, a.seg_chunks = IMPL[impl], int(p_block), int(seg_chunks)
     a.head_block = int(head_block)
     return int(lib.ssd_chunk_scan_workspace_size(ctypes.byref(a)))
+
+
+def chunk_scan_gated_norm_workspace_size(x, B, C, z, norm_weight, out, *, cu_seqlens,
+                                         chunk_size, group_size, y=None, impl="auto",
+                                         p_block=0, seg_chunks=0, head_block=0):
+    """Bytes of workspace chunk_scan_gated_norm wants for these tensors
+    (ssd_chunk_scan_gated_norm_workspace_size in ssd.h): the split of the scan when its
+    planner splits, else the ready queue of the overlapped form, else 0."""
+    lib = load_library()
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    a = ScanArgs()
+    a.struct_size = ctypes.sizeof(ScanArgs)
+    a.x, a.x_stride_t = _ptr(x), _token_stride(x, "x", H * P)
+    a.B, a.B_stride_t = _ptr(B), _token_stride(B, "B", G * N)
+    a.C, a.C_stride_t = _ptr(C), _token_stride(C, "C", G * N)
+    a.dt = a.A = a.x
+    a.y = _ptr(y)
+    a.cu_seqlens = _ptr(cu_seqlens)
+    a.nseq, a.T, a.H, a.P, a.G, a.N = cu_seqlens.shape[0] - 1, T, H, P, G, N
+    a.chunk_size, a.act_dtype = int(chunk_size), _act(x)
+    a.impl, a.p_block, a.seg_chunks = IMPL[impl], int(p_block), int(seg_chunks)
+    a.head_block = int(head_block)
+    return int(lib.ssd_chunk_scan_gated_norm_workspace_size(
+        ctypes.byref(a), _ptr(z), _ptr(norm_weight), int(group_size), _ptr(out)))
 
 
 def _update_args(state_pool, state_indices, x, dt, A, B, C, D, dt_bias, dt_softplus, y,

@@ -23,6 +23,7 @@ def test_exports_every_declared_entry_point(lib):
     names = ssd.header_functions()
     assert set(names) == {"ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
                           "ssd_chunk_scan_static_ws", "ssd_chunk_scan_gated_norm",
+                          "ssd_chunk_scan_gated_norm_workspace_size",
                           "ssd_state_update", "ssd_state_update_multi", "ssd_decode_layer_step",
                           "ssd_state_copy", "gated_rmsnorm", "ssd_read_status",
                           "ssd_status_string", "ssd_version"}
@@ -139,6 +140,52 @@ def test_scan_workspace_size(lib):
     assert size(nseq=1, T=16384, H=128, G=8) == 0
     assert size(nseq=1, T=65536, H=128, G=8) == 0
     assert lib.ssd_chunk_scan_workspace_size(None) == 0
+
+
+def test_scan_gated_norm_workspace_size(lib):
+    """Host-side planning only: no kernel runs.  The overlapped scan + norm (two heads per
+    CTA, unsplit, bf16, groups of whole 64-channel head blocks, 16-byte aligned rows, at
+    most two waves of CTAs) wants its ready queue: per chunk id (ceil(T/128) + nseq of
+    them) and norm group, one int count and four 8-byte task slots, plus four ints,
+    rounded up to 256 bytes (norm groups the vector norm takes: 8 x 32 x v channels, v
+    <= 4, and multiples).  A split the planner would choose takes the workspace
+    instead; anything the overlapped form cannot take wants none."""
+    lib.ssd_chunk_scan_gated_norm_workspace_size.argtypes = [
+        ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p]
+    lib.ssd_chunk_scan_gated_norm_workspace_size.restype = ctypes.c_size_t
+    kw = dict(act_dtype=ssd.SSD_BF16, nseq=4, T=16384, H=128, P=64, G=8, N=128, chunk_size=128)
+    r256 = lambda b: (b + 255) // 256 * 256
+    queue = lambda T, nseq, ngroups: r256(((T + 127) // 128 + nseq) * ngroups * (4 + 4 * 8)
+                                          + 16)
+
+    def size(gs=1024, z=0x200000, w=0x300000, out=0x400000, y=0x100000, **o):
+        a = _scan_args(**{**kw, **o})
+        a.y = y
+        return lib.ssd_chunk_scan_gated_norm_workspace_size(
+            ctypes.byref(a), ctypes.c_void_p(z), ctypes.c_void_p(w), gs, ctypes.c_void_p(out))
+
+    # the Nemotron-H-shaped varlen prefill: 256 pair CTAs, norm groups of 16 heads
+    assert size() == queue(16384, 4, 8)
+    assert size(head_block=2) == queue(16384, 4, 8)
+    assert size(gs=256) == queue(16384, 4, 32)
+    assert size(z=0) == queue(16384, 4, 8)              # no gate
+    assert size(y=0) == queue(16384, 4, 8)              # y written into out
+    assert size(gs=8192, H=128) == queue(16384, 4, 1)
+    # anything else runs the norm after the scan and wants no queue
+    assert size(gs=128) == 0                             # no vector norm for 16 vectors
+    assert size(gs=96 * 8) == 0                          # group of 12.5 64-channel blocks
+    assert size(z=0x200008) == 0                         # z rows not 16-byte aligned
+    assert size(head_block=1) == 0                       # one head per CTA
+    assert size(impl=1) == 0                             # SIMT scan
+    assert size(act_dtype=ssd.SSD_F32) == 0              # fp32: no tensor-core scan
+    assert size(nseq=8, T=32768) == 0                    # 512 CTAs: more than two waves
+    assert size(T=0) == 0
+    assert size(gs=0) == 0 and size(gs=1000) == 0        # invalid group sizes
+    # a split the planner is told to make takes the workspace (the norm then follows)
+    split = lib.ssd_chunk_scan_workspace_size(ctypes.byref(_scan_args(**kw, seg_chunks=4)))
+    assert split > 0 and size(seg_chunks=4) == split
+    assert lib.ssd_chunk_scan_gated_norm_workspace_size(None, None, None, 1024, None) == 0
 
 
 def test_update_rejects_bad_arguments(lib):

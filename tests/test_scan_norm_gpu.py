@@ -70,12 +70,13 @@ def _fused(s, n, gs, *, want_y, seg_chunks=0, z=True, graph=False):
     return out, y, fs, bits
 
 
-def _separate(s, n, gs, *, seg_chunks=0, z=True):
+def _separate(s, n, gs, *, seg_chunks=0, z=True, head_block=0):
     d = _dev_inputs(s)
     y, fs = ssd.chunk_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=d["cu_seqlens"],
                            chunk_size=s.chunk_size, D=d["D"], dt_bias=d["dt_bias"],
                            initial_states=d["initial_states"],
-                           has_initial_state=d["has_initial_state"], seg_chunks=seg_chunks)
+                           has_initial_state=d["has_initial_state"], seg_chunks=seg_chunks,
+                           head_block=head_block)
     T, H, P = y.shape
     out = ssd.gated_rmsnorm(y.view(T, H * P), dev(n.z) if z else None, dev(n.weight),
                             group_size=gs, eps=n.eps)
@@ -245,3 +246,158 @@ def test_layer_mixed_nemotron_h_shapes_with_concurrent_decode():
     assert st == 0
     check_bf16("mixed decode y", uy.float().cpu().numpy(), yr_dec)
     check_bf16("mixed decode pool", pool.cpu().numpy(), ref_pool)
+
+
+# The overlapped form: the scan (two heads per CTA, unsplit) appends each finished
+# 128-token chunk of each norm group to a queue in the workspace, and the norm, launched
+# as a programmatic dependent, normalises those rows while the scan runs on.  Each case is
+# checked to take that form (its workspace is the ready queue), then held bit for bit to
+# the chained form of the same call, to the two plain calls and to the oracle.
+OVERLAP_CASES = {
+    # ragged varlen with empty and one-token sequences: one group of 4 heads (2 CTAs)
+    "varlen_one_group_of_4_heads": (
+        lambda: I.make_scan_inputs([700, 129, 1, 0, 300, 1000, 257, 128, 385], H=4, P=64,
+                                   G=2, N=128, chunk_size=256, act="bf16", seed=211,
+                                   init="all"), 256),
+    # 16 heads in 4 groups of 4 heads: two CTAs per group, four groups per row
+    "groups_of_4_heads": (
+        lambda: I.make_scan_inputs([513, 64, 1300], H=16, P=64, G=2, N=128, chunk_size=128,
+                                   act="bf16", seed=213, init=[1, 0, 1]), 256),
+    # P = 128: each CTA's two 64-channel head blocks lie in two different groups
+    "p128_head_blocks_in_two_groups": (
+        lambda: I.make_scan_inputs([400, 777], H=4, P=128, G=1, N=128, chunk_size=128,
+                                   act="bf16", seed=215, init="all"), 256),
+    # one group over all 1536 channels of the Mamba2-130M shape: 12 CTAs per group
+    "mamba2_130m_one_group": (lambda: I.scan_workload("mamba2_130m"), 1536),
+}
+
+
+def _overlap_call(s, n, gs, *, workspace, want_y, z=True, status=None):
+    d = _dev_inputs(s)
+    T, H, P = d["x"].shape
+    zt, wt = (dev(n.z) if z else None), dev(n.weight)
+    y = _nan((T, H, P), d["x"].dtype) if want_y else None
+    out = _nan((T, H * P), d["x"].dtype)
+    fs = _nan((s.nseq, H, P, s.N), torch.float32)
+    status = ssd.new_status() if status is None else status
+    ssd.chunk_scan_gated_norm(d["x"], d["dt"], d["A"], d["B"], d["C"], zt, wt,
+                              cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size,
+                              group_size=gs, eps=n.eps, D=d["D"], dt_bias=d["dt_bias"],
+                              initial_states=d["initial_states"],
+                              has_initial_state=d["has_initial_state"], y=y, out=out,
+                              final_states=fs, status=status, seg_chunks=-1, head_block=2,
+                              workspace=workspace)
+    _, bits = ssd.read_status(status)
+    return out, y, fs, bits
+
+
+def _queue_bytes(s, d_channels, gs):
+    nid = -(-s.T // 128) + s.nseq
+    return (nid * (d_channels // gs) * (4 + 4 * 8) + 16 + 255) // 256 * 256
+
+
+def _takes_overlapped_form(s, n, gs, z=True):
+    d = _dev_inputs(s)
+    T, H, P = d["x"].shape
+    out = torch.empty((T, H * P), dtype=d["x"].dtype, device="cuda")
+    nws = ssd.chunk_scan_gated_norm_workspace_size(
+        d["x"], d["B"], d["C"], dev(n.z) if z else None, dev(n.weight), out,
+        cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size, group_size=gs, seg_chunks=-1,
+        head_block=2)
+    return nws == _queue_bytes(s, H * P, gs), nws
+
+
+@pytest.mark.parametrize("case", sorted(OVERLAP_CASES))
+@pytest.mark.parametrize("want_y", [True, False])
+def test_overlapped_scan_gated_norm(case, want_y):
+    make, gs = OVERLAP_CASES[case]
+    s = make()
+    n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=217)
+    ok, nws = _takes_overlapped_form(s, n, gs)
+    assert ok, f"not the overlapped form (workspace {nws})"
+    out, y, fs, bits = _overlap_call(s, n, gs, workspace=None, want_y=want_y)
+    assert bits == 0
+    chained = torch.empty(0, dtype=torch.uint8, device="cuda")   # too small: the chained form
+    out_c, y_c, fs_c, bits_c = _overlap_call(s, n, gs, workspace=chained, want_y=want_y)
+    assert bits_c == 0
+    out_sep, y_sep, fs_sep = _separate(s, n, gs, seg_chunks=-1, head_block=2)
+    assert torch.equal(out, out_c), "overlapped and chained forms differ"
+    assert torch.equal(out, out_sep), "differs from the two plain calls"
+    assert torch.equal(fs, fs_c) and torch.equal(fs, fs_sep)
+    if want_y:
+        assert torch.equal(y, y_c) and torch.equal(y, y_sep)
+    yr, fr, outr = _oracle(s, n, gs)
+    T = yr.shape[0]
+    carried = norm_carried_rounding(yr.reshape(T, -1), n.z.values, n.weight.values, gs, n.eps)
+    check_bf16(f"overlapped {case} out", out.float().cpu().numpy(), outr, stored_bf16=True,
+               carried=carried)
+    check_bf16(f"overlapped {case} final", fs.cpu().numpy(), fr)
+
+
+def test_overlapped_no_gate_and_in_a_cuda_graph():
+    """No gate, captured once and replayed twice from NaN outputs: the queue is zeroed by
+    the call itself on every replay, and each replay equals the two plain calls."""
+    make, gs = OVERLAP_CASES["groups_of_4_heads"]
+    s = make()
+    n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=219)
+    assert _takes_overlapped_form(s, n, gs, z=False)[0]
+    d = _dev_inputs(s)
+    T, H, P = d["x"].shape
+    wt = dev(n.weight)
+    out = _nan((T, H * P), d["x"].dtype)
+    fs = _nan((s.nseq, H, P, s.N), torch.float32)
+    status = ssd.new_status()
+    ws = torch.empty(_takes_overlapped_form(s, n, gs, z=False)[1], dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        ssd.chunk_scan_gated_norm(d["x"], d["dt"], d["A"], d["B"], d["C"], None, wt,
+                                  cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size,
+                                  group_size=gs, eps=n.eps, D=d["D"], dt_bias=d["dt_bias"],
+                                  initial_states=d["initial_states"],
+                                  has_initial_state=d["has_initial_state"], out=out,
+                                  final_states=fs, status=status, seg_chunks=-1,
+                                  head_block=2, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    with torch.cuda.stream(s2):
+        with torch.cuda.graph(g, stream=s2):
+            call()
+    torch.cuda.synchronize()
+    out_sep, _, fs_sep = _separate(s, n, gs, seg_chunks=-1, z=False, head_block=2)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        fs.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out_sep)
+        assert torch.equal(fs, fs_sep)
+    _, bits = ssd.read_status(status)
+    assert bits == 0
+
+
+def test_overlapped_heads_with_A_not_negative():
+    """Head pair 0 has both A >= 0 (its CTAs write zero rows and count every chunk at once),
+    head 5 alone of its pair: the status bit is raised, the norm still receives every
+    chunk, and the call equals its chained form bit for bit."""
+    s = I.make_scan_inputs([600, 37, 900], H=8, P=64, G=2, N=128, chunk_size=128,
+                           act="bf16", seed=221, init="all")
+    A = s.A.values.copy()
+    A[0], A[1], A[5] = 0.0, np.nan, 0.5
+    s.A = I.Tensor(A, "f32")
+    gs = 256
+    n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=223)
+    assert _takes_overlapped_form(s, n, gs)[0]
+    out, _, fs, bits = _overlap_call(s, n, gs, workspace=None, want_y=False)
+    assert bits & ssd.DEV_A_NOT_NEG
+    out_c, _, fs_c, bits_c = _overlap_call(s, n, gs, workspace=torch.empty(0, dtype=torch.uint8,
+                                                                            device="cuda"),
+                                           want_y=False)
+    assert bits_c & ssd.DEV_A_NOT_NEG
+    assert torch.equal(out, out_c)
+    assert torch.equal(fs, fs_c)
+    assert not torch.isnan(out).any()

@@ -37,6 +37,14 @@ def fault_lib():
     lib = ctypes.CDLL(path)
     lib.ssd_chunk_scan.argtypes = [ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p]
     lib.ssd_chunk_scan.restype = ctypes.c_int
+    lib.ssd_chunk_scan_gated_norm.argtypes = [ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int32,
+                                              ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    lib.ssd_chunk_scan_gated_norm.restype = ctypes.c_int
+    lib.ssd_chunk_scan_gated_norm_workspace_size.argtypes = [
+        ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p]
+    lib.ssd_chunk_scan_gated_norm_workspace_size.restype = ctypes.c_size_t
     lib.ssd_test_withhold_chunk.argtypes = [ctypes.c_int]
     lib.ssd_test_withhold_chunk.restype = ctypes.c_int
     yield lib
@@ -100,3 +108,52 @@ def test_withheld_chunk_times_out_and_context_survives(fault_lib):
     y_ref, f_ref = scan_oracle(s)
     check_bf16("after timeout y", y_gpu, y_ref)
     check_bf16("after timeout final", f_gpu, f_ref)
+
+
+def test_overlapped_norm_stops_waiting_when_the_scan_aborts(fault_lib):
+    """The scan + norm call in its overlapped form (the norm drains a queue the scan fills
+    as it runs): when the scan gives up on a withheld chunk, it raises the queue's abort
+    flag, the norm's blocks stop waiting for the chunks that will not come, and the call
+    ends with SSD_DEV_TIMEOUT on a context that still runs the regular library."""
+    # 4 heads (two head pairs), one norm group over their 256 channels
+    s = I.make_scan_inputs([600], H=4, P=64, G=2, N=128, chunk_size=256, act="bf16",
+                           seed=911, init="none")
+    x, dt, A, Bm, C, D, bias = (dev(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D, s.dt_bias))
+    cu = torch.from_numpy(s.cu_seqlens).cuda()
+    T, d = s.T, s.H * s.P
+    nrm = I.make_norm_inputs(T, d, d, act="bf16", seed=909)
+    z, w = dev(nrm.z), dev(nrm.weight)
+    out = torch.zeros((T, d), dtype=torch.bfloat16, device="cuda")
+    fs = torch.zeros((s.nseq, s.H, s.P, s.N), device="cuda")
+    status = ssd.new_status()
+    a = scan_args_struct(x, dt, A, Bm, C, cu, s.chunk_size, D=D, dt_bias=bias, fs=fs,
+                         status=status, seg_chunks=-1, head_block=2)
+    a.impl = 2
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    nws = fault_lib.ssd_chunk_scan_gated_norm_workspace_size(ctypes.byref(a), ptr(z), ptr(w),
+                                                            d, ptr(out))
+    assert nws > 0, "the case must take the overlapped form"
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    a.workspace, a.workspace_bytes = ws.data_ptr(), nws
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert fault_lib.ssd_test_withhold_chunk(1) == 0
+    try:
+        rc = fault_lib.ssd_chunk_scan_gated_norm(ctypes.byref(a), ptr(z), ptr(w), ssd.SSD_BF16,
+                                                 d, ctypes.c_float(1e-5), ptr(out), stream)
+        assert rc == 0
+        rc, bits = ssd.read_status(status)
+    finally:
+        fault_lib.ssd_test_withhold_chunk(-1)
+    assert bits & 0x8, f"SSD_DEV_TIMEOUT not raised (bits={bits:#x})"
+    assert rc == 7
+    assert torch.cuda.synchronize() is None
+
+    # the same context: the regular library's overlapped call equals its plain calls
+    out2, _ = ssd.chunk_scan_gated_norm(x, dt, A, Bm, C, z, w, cu_seqlens=cu,
+                                        chunk_size=s.chunk_size, group_size=d, D=D,
+                                        dt_bias=bias, seg_chunks=-1, head_block=2)
+    y_sep, _ = ssd.chunk_scan(x, dt, A, Bm, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=D,
+                              dt_bias=bias, seg_chunks=-1, head_block=2)
+    out_sep = ssd.gated_rmsnorm(y_sep.view(T, d), z, w, group_size=d)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out_sep)
