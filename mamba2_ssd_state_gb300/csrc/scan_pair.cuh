@@ -44,8 +44,11 @@ constexpr int PBP = 64;                 // channels per head in a CTA
 constexpr int kPairMaskWarps = 8, kPairStateWarps = 4, kPairEpiWarps = 4;
 constexpr int kDecay0 = 2, kMask0 = 4, kState0 = kMask0 + kPairMaskWarps;
 constexpr int kEpi0 = kState0 + kPairStateWarps;
-constexpr int kPub = kEpi0 + kPairEpiWarps;  // the ready-queue publisher (one lane)
-constexpr int kPairThreads = 32 * (kPub + 1);
+constexpr int kPairThreads = 32 * (kEpi0 + kPairEpiWarps);
+// the scan of the scan + norm call adds one warp, the ready-queue publisher (its own
+// instantiation: with 21 warps the register budget per thread drops from 96 to 80)
+constexpr int kPub = kEpi0 + kPairEpiWarps;
+template <bool kReady> constexpr int pair_threads() { return kPairThreads + (kReady ? 32 : 0); }
 constexpr int kTile = 16384;            // one head's [128 rows][64] bf16 tile
 constexpr int kB = 0;                   // B tile, two 64-wide 128B-swizzled boxes
 constexpr int kC = 32768;               // C tile
@@ -54,7 +57,7 @@ constexpr int kXs = kX + 4 * kTile;     // w o x, 2 heads
 constexpr int kHT = kXs + 2 * kTile;    // h^T bf16, 2 heads: [n rows][64 p]
 constexpr int kPro = kHT + 2 * kTile;   // float [NB][2][kProStride]
 constexpr int kBar = kPro + NB * 2 * kProStride * 4;
-constexpr int kNumBar = 2 * 2 + 2 + 2 + 2 * NB + 14;
+constexpr int kNumBar = 2 * 2 + 2 + 2 + 2 * NB + 11;
 constexpr int kFlags = kBar + kNumBar * 8;
 constexpr int kSmemBytes = kFlags + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
@@ -66,7 +69,7 @@ constexpr uint32_t kColPCB = 0, kColY = 128, kColH = 256, kColO = 384;
 // kReady: the unsplit scan of the scan + norm call, which fills the norm's ready queue
 // (a separate instantiation: the queue code costs the plain scan time even unexecuted).
 template <bool kSplit, bool kReady = false>
-__global__ void __launch_bounds__(pair::kPairThreads, 1)
+__global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     scan_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const TcParams prm) {
   using namespace pair;
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
   for (int e = 0; e < 2; ++e) {
     if (!(e ? bad1 : bad0) || !prm.fin || kseg != 0) continue;
     float* fin = prm.fin + ((size_t)s * H + h0 + e) * PN + (size_t)p0 * NSTATE;
-    for (int i = threadIdx.x; i < PBP * NSTATE; i += kPairThreads) fin[i] = 0.f;
+    for (int i = threadIdx.x; i < PBP * NSTATE; i += pair_threads<kReady>()) fin[i] = 0.f;
   }
   // the scan + norm call: where this CTA's two 64-channel head blocks lie among the norm
   // groups, and the id of the sequence's first chunk (unsplit: tb is the sequence start)
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
     }
   };
   if (bad0 && bad1) {
-    for (int e = threadIdx.x; e < (te - tb) * 2 * PBP; e += kPairThreads) {
+    for (int e = threadIdx.x; e < (te - tb) * 2 * PBP; e += pair_threads<kReady>()) {
       const int tok = tb + e / (2 * PBP), hh = h0 + (e / PBP) % 2;
       prm.y[((size_t)tok * H + hh) * P + p0 + e % PBP] = __float2bfloat16_rn(0.f);
     }
@@ -182,10 +185,8 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
   uint64_t* h_ready = cb_full + 6;       //      scaled state in TMEM, h^T in smem (4 state)
   uint64_t* y_empty = cb_full + 7;       //      Y and Yoff read (4 epilogue warps)
   uint64_t* drain = cb_full + 8;         //      teardown: all MMAs retired
-  // scan + norm call: chunk parity k's rows written (4 output warps); published (publisher)
-  uint64_t* y_pub = cb_full + 9;         // [2]
-  uint64_t* pub_done = cb_full + 11;     // [2]
-  static_assert(kNumBar == 8 + 2 * NB + 14, "barrier block size");
+  uint64_t* pub_done = cb_full + 9;      //      scan + norm call: chunk published
+  static_assert(kNumBar == 8 + 2 * NB + 11, "barrier block size");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kFlags + 4);
 
@@ -211,10 +212,7 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
     mbar_init(h_ready, kPairStateWarps);
     mbar_init(y_empty, kPairEpiWarps);
     mbar_init(drain, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&y_pub[i], kPairEpiWarps);
-      mbar_init(&pub_done[i], 1);
-    }
+    mbar_init(pub_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     // thread 0 is the TMA producer: chunk 0's tiles (and chunk 1's x) are on their way
@@ -327,18 +325,29 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
       for (int c = nx > 2 ? nx - 2 : 0; c < nx; ++c)
         mbar_wait_drain(&x_full[c & 1], (c >> 1) & 1, kWaitLimit);
     }
-  } else if (warp == kPub) {
+  } else if (kReady && warp == kPub) {
     if (lane == 0 && ready) {
       // the publisher of the scan + norm call: once the four output warps have written
-      // chunk cc (their arrivals on y_pub release their stores to this CTA), make those
-      // rows visible to the whole GPU and count them in the norm's ready queue, then free
-      // the barrier phase for chunk cc + 2.  The atomics' round trips stay off the output
-      // warps.
+      // chunk cc (their y_empty arrivals release their stores to this CTA), make those
+      // rows visible to the whole GPU, count them in the norm's ready queue and tell the
+      // output warps (who wait for it before they finish chunk cc + 1, so y_empty is never
+      // two phases ahead of this loop).  The atomics' round trips stay off the output
+      // warps; the barrier is polled with sleeps, the cheapest way to watch it.
       for (int cc = 0; cc < nch; ++cc) {
-        if (!mbar_wait(&y_pub[cc & 1], (cc >> 1) & 1, abort_flag, kWaitLimit)) break;
+        const long long t0 = clock64();
+        bool ok = true;
+        while (!mbar_test_wait(y_empty, cc & 1)) {
+          if (*abort_flag || clock64() - t0 > kWaitLimit) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (!ok) break;
         __threadfence();
         publish(cc, kPairEpiWarps);
-        mbar_arrive(&pub_done[cc & 1]);
+        mbar_arrive(pub_done);
       }
     }
   } else if (warp >= kDecay0 && warp < kMask0) {
@@ -738,8 +747,6 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
       if (!wwait(o_full, c & 1)) break;
       if (!wwait(&x_full[sx], (c >> 1) & 1)) break;
       if (!wwait(&pro_full[b], (c / NB) & 1)) break;
-      // the publisher is done with chunk c - 2, whose barrier phase chunk c reuses
-      if (ready && c >= 2 && !wwait(&pub_done[c & 1], ((c >> 1) - 1) & 1)) break;
       tc_fence_after();
       const int tok = tb + c * QT + r;
 #pragma unroll 1
@@ -779,12 +786,13 @@ __global__ void __launch_bounds__(pair::kPairThreads, 1)
         }
       }
       tc_fence_before();
+      // chunk c - 1 is published, so the publisher has seen y_empty's previous phase
+      if (ready && c >= 1 && !wwait(pub_done, (c - 1) & 1)) break;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(y_empty);
         mbar_arrive(&x_empty[sx]);
         mbar_arrive(&pro_empty[b]);
-        if (ready) mbar_arrive(&y_pub[c & 1]);  // this warp's rows of chunk c (release)
       }
     }
   }

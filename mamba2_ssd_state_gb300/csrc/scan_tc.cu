@@ -1377,7 +1377,7 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   }
   const long long grid = plan.nseg * (a.H / plan.hb) * prm.npb;
   if (pair && rq) {
-    scan_pair_kernel<false, true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
+    scan_pair_kernel<false, true><<<(unsigned)grid, pair::pair_threads<true>(), pair::kSmemBytes, st>>>(mX, mB, mC, prm);
   } else if (pair) {
     if (split)
       scan_pair_kernel<true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
