@@ -76,6 +76,10 @@ constexpr int NB = 3;            // depth of the decay buffer ring
 constexpr int kMaskWarps = 8, kOutWarps = 4;
 constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
 constexpr int kThreads = 32 * (kDecayWarp + 1);
+// the scan of the scan + norm call (kReady) adds warp kDecayWarp + 1, the ready-queue
+// publisher; with 16 warps the register budget per thread stays at 128
+constexpr int kPubWarp = kDecayWarp + 1;
+template <bool kReady> constexpr int tc_threads() { return kThreads + (kReady ? 32 : 0); }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFactorLimit = 64.f;            // log2 bound of a factorised decay factor
 constexpr long long kWaitLimit = SSD_WAIT_LIMIT_CYCLES;  // SM cycles a wait may take
@@ -131,7 +135,7 @@ struct Layout {
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
   static constexpr int kPro = kHT + 2 * kHTPad;        // float [NB][kProStride]
   static constexpr int kBar = kPro + NB * kProStride * 4;
-  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS;
+  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 13 + 3 * NXS;
   static constexpr int kFlags = kBar + kNumBar * 8;    // abort flag, TMEM base
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
@@ -152,8 +156,10 @@ __device__ __forceinline__ float softplus_fast(float v) {
   return v < -8.f ? e : __logf(1.f + e);
 }
 
-template <int PB, bool kSplit>
-__global__ void __launch_bounds__(kThreads, 1)
+// kReady: the unsplit scan of the scan + norm call, which fills the norm's ready queue
+// (64-channel blocks only; its own instantiation).
+template <int PB, bool kSplit, bool kReady = false>
+__global__ void __launch_bounds__(tc_threads<kReady>(), 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams prm) {
   using L = Layout<PB>;
@@ -215,16 +221,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split) return prm.ws_h + ((size_t)j * H + h) * PN + (size_t)p0 * NSTATE;
     return prm.fin ? prm.fin + ((size_t)s * H + h) * PN + (size_t)p0 * NSTATE : nullptr;
   };
+  // the scan + norm call: this CTA's norm group, the id of the sequence's first chunk
+  // (unsplit: tb is the sequence start), and the count of chunk cc's rows of y
+  const bool ready = kReady && !kSplit && PB == 64 && prm.rq.cnt != nullptr;
+  const int grp = ready ? (h * P + p0) / prm.rq.gs : 0;
+  const long long id0 = (long long)(tb / QT) + s;
   if (!(Ah < 0.f)) {  // sign test (NaN, +0, -0 fail): the chain produces zeros
     if (threadIdx.x == 0 && pbk == 0 && kseg == 0) set_status(prm.status, SSD_DEV_A_NOT_NEG);
-    for (int e = threadIdx.x; e < (te - tb) * PB; e += kThreads)
+    for (int e = threadIdx.x; e < (te - tb) * PB; e += tc_threads<kReady>())
       prm.y[((size_t)(tb + e / PB) * H + h) * P + p0 + e % PB] = __float2bfloat16_rn(0.f);
     // the first segment zeroes the final state (the fix-up kernel skips such heads)
     float* fin = (prm.fin && kseg == 0)
                      ? prm.fin + ((size_t)s * H + h) * PN + (size_t)p0 * NSTATE
                      : nullptr;
     if (fin)
-      for (int e = threadIdx.x; e < PB * NSTATE; e += kThreads) fin[e] = 0.f;
+      for (int e = threadIdx.x; e < PB * NSTATE; e += tc_threads<kReady>()) fin[e] = 0.f;
+    if (ready) {  // the zero rows count for every chunk at once
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0)
+        for (int cc = 0; cc < nch; ++cc)
+          ready_publish(prm.rq, id0 + cc, s, cc, grp, kOutWarps);
+    }
     return;
   }
 
@@ -251,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* yoff_full = h_ready + 2;        // [2]   Yoff buffer done
   uint64_t* y_empty = yoff_full + 2;        // [2]   Y and Yoff buffers read (4 output warps)
   uint64_t* drain = y_empty + 2;            //       teardown: all MMAs retired
-  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS,
+  uint64_t* pub_done = drain + 1;           //       scan + norm call: chunk published
+  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 13 + 3 * NXS,
                 "barrier block size must match the barriers laid out here");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
@@ -288,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&y_empty[i], kOutWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(pub_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     // thread 0 is the TMA producer: chunk 0's tiles are on their way while the rest of
@@ -382,6 +402,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(&c_full[c % NBC], (c / NBC) & 1, kWaitLimit);
       for (int c = nx_iss > NX ? nx_iss - NX : 0; c < nx_iss; ++c)
         mbar_wait_drain(&x_full[c % NX], (c / NX) & 1, kWaitLimit);
+    }
+  } else if (kReady && warp == kPubWarp) {
+    if (lane == 0 && ready) {
+      // the publisher of the scan + norm call: once the four output warps have written
+      // chunk cc (their y_empty arrivals release their stores to this CTA), make those
+      // rows visible to the whole GPU, count them in the norm's ready queue and tell the
+      // output warps, who wait for it before they finish chunk cc + 1 (so y_empty of a
+      // buffer is never a phase ahead of this loop)
+      for (int cc = 0; cc < nch; ++cc) {
+        const long long t_wait = clock64();
+        bool ok = true;
+        while (!mbar_test_wait(&y_empty[cc & 1], (cc >> 1) & 1)) {
+          if (*abort_flag || clock64() - t_wait > kWaitLimit) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (!ok) break;
+        __threadfence();
+        ready_publish(prm.rq, id0 + cc, s, cc, grp, kOutWarps);
+        mbar_arrive(pub_done);
+      }
     }
   } else if (warp == kDecayWarp) {
     // ------------------------------------------------------------ decay warp
@@ -753,6 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
+      // chunk c - 1 is published, so the publisher has seen y_empty's previous phase
+      if (ready && c >= 1 && !(ok = wwait(pub_done, (c - 1) & 1))) break;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&y_empty[c & 1]);
@@ -773,7 +819,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && *abort_flag) set_status(prm.status, SSD_DEV_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_flag) {
+    set_status(prm.status, SSD_DEV_TIMEOUT);
+    if (ready) atomicExch(prm.rq.abort, 1);  // the norm stops waiting for these rows
+  }
 }
 
 #ifdef SSD_FAULT_INJECT
@@ -1334,7 +1383,7 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   // dynamic shared memory above 48 KB is opted into once per kernel and device
   static std::atomic<bool> set_one[kMaxDevices], set_one_split[kMaxDevices],
       set_pair[kMaxDevices], set_pair_split[kMaxDevices], set_pair_ready[kMaxDevices],
-      set_fix[kMaxDevices];
+      set_one_ready[kMaxDevices], set_fix[kMaxDevices];
   const bool split = plan.segc > 0;
   bool ok;
   if (pair && rq)
@@ -1342,7 +1391,10 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   else if (pair)
     ok = split ? opt_in(scan_pair_kernel<true>, pair::kSmemBytes, set_pair_split)
                : opt_in(scan_pair_kernel<false>, pair::kSmemBytes, set_pair);
-  else
+  else if (rq) {
+    if constexpr (PB == 64) ok = opt_in(scan_tc_kernel<PB, false, true>, L::kSmemBytes, set_one_ready);
+    else return SSD_ERR_UNSUPPORTED;
+  } else
     ok = split ? opt_in(scan_tc_kernel<PB, true>, L::kSmemBytes, set_one_split)
                : opt_in(scan_tc_kernel<PB, false>, L::kSmemBytes, set_one);
   if (ok && split) ok = opt_in(scan_fixup_kernel<PB>, FixLayout<PB>::kSmemBytes, set_fix);
@@ -1372,7 +1424,7 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   prm.segc = plan.segc;
   prm.rq = ReadyQueue{};
   if (rq) {
-    if (!pair || split) return SSD_ERR_UNSUPPORTED;
+    if (split || PB != 64) return SSD_ERR_UNSUPPORTED;
     prm.rq = *rq;
   }
   const long long grid = plan.nseg * (a.H / plan.hb) * prm.npb;
@@ -1383,6 +1435,9 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
       scan_pair_kernel<true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
     else
       scan_pair_kernel<false><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
+  } else if (rq) {
+    if constexpr (PB == 64)
+      scan_tc_kernel<PB, false, true><<<(unsigned)grid, tc_threads<true>(), L::kSmemBytes, st>>>(mX, mB, mC, prm);
   } else {
     if (split)
       scan_tc_kernel<PB, true><<<(unsigned)grid, kThreads, L::kSmemBytes, st>>>(mX, mB, mC, prm);
@@ -1489,8 +1544,8 @@ constexpr int kReadyMaxWaves = 2;
 bool scan_tc_ready_plan(const ssd_scan_args& a) {
   if (!scan_tc_supported(a)) return false;
   ScanPlan plan;
-  if (final_plan(a, SIZE_MAX, &plan) != SSD_OK || plan.hb != 2 || plan.segc != 0) return false;
-  const long long grid = (long long)a.nseq * (a.H / 2) * (a.P / 64);
+  if (final_plan(a, SIZE_MAX, &plan) != SSD_OK || plan.pb != 64 || plan.segc != 0) return false;
+  const long long grid = (long long)a.nseq * (a.H / plan.hb) * (a.P / 64);
   return grid <= (long long)kReadyMaxWaves * sm_count();
 }
 
@@ -1498,7 +1553,7 @@ ssd_status launch_scan_tc_ready(const ssd_scan_args& a, const ReadyQueue& rq, cu
   ScanPlan plan;
   const ssd_status v = final_plan(a, SIZE_MAX, &plan);
   if (v != SSD_OK) return v;
-  if (plan.hb != 2 || plan.segc != 0) return SSD_ERR_UNSUPPORTED;
+  if (plan.pb != 64 || plan.segc != 0) return SSD_ERR_UNSUPPORTED;
   return launch_pb<64>(a, plan, st, &rq);
 }
 

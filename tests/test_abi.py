@@ -149,7 +149,8 @@ def test_scan_gated_norm_workspace_size(lib):
     them) and norm group, one int count and four 8-byte task slots, plus four ints,
     rounded up to 256 bytes (norm groups the vector norm takes: 8 x 32 x v channels, v
     <= 4, and multiples).  A split the planner would choose takes the workspace
-    instead; anything the overlapped form cannot take wants none."""
+    instead; anything the overlapped form cannot take (or fewer than 4096 tokens) wants
+    none."""
     lib.ssd_chunk_scan_gated_norm_workspace_size.argtypes = [
         ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
         ctypes.c_void_p]
@@ -176,11 +177,21 @@ def test_scan_gated_norm_workspace_size(lib):
     assert size(gs=128) == 0                             # no vector norm for 16 vectors
     assert size(gs=96 * 8) == 0                          # group of 12.5 64-channel blocks
     assert size(z=0x200008) == 0                         # z rows not 16-byte aligned
-    assert size(head_block=1) == 0                       # one head per CTA
+    assert size(head_block=1) == 0                       # one head per CTA: 512 CTAs
+    # a single 16K-token sequence: one head (128 CTAs) or two (64) per CTA both qualify
+    # unsplit; told it may split, the two-head plan splits (the split takes the workspace)
+    assert size(nseq=1, head_block=1) == queue(16384, 1, 8)
+    assert size(nseq=1, head_block=2, seg_chunks=-1) == queue(16384, 1, 8)
+    one = dict(kw, nseq=1, head_block=2)
+    assert size(nseq=1, head_block=2) == lib.ssd_chunk_scan_workspace_size(
+        ctypes.byref(_scan_args(**one))) > 0
+    assert size(nseq=1, head_block=1, p_block=32) == 0   # 32-channel blocks
     assert size(impl=1) == 0                             # SIMT scan
     assert size(act_dtype=ssd.SSD_F32) == 0              # fp32: no tensor-core scan
     assert size(nseq=8, T=32768) == 0                    # 512 CTAs: more than two waves
     assert size(T=0) == 0
+    assert size(nseq=1, T=4095) == 0                     # short: the norm follows the scan
+    assert size(nseq=1, T=4096) == queue(4096, 1, 8)
     assert size(gs=0) == 0 and size(gs=1000) == 0        # invalid group sizes
     # a split the planner is told to make takes the workspace (the norm then follows)
     split = lib.ssd_chunk_scan_workspace_size(ctypes.byref(_scan_args(**kw, seg_chunks=4)))

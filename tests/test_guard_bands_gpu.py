@@ -118,18 +118,18 @@ def test_scan_gated_norm_outputs_stay_in_bounds(with_y):
     torch.testing.assert_close(fs.t, f_ref, rtol=0, atol=0)
 
 
-@pytest.mark.parametrize("with_y", [True, False])
-def test_overlapped_scan_gated_norm_stays_in_bounds(with_y):
+@pytest.mark.parametrize("with_y,hb", [(True, 2), (False, 2), (True, 1)])
+def test_overlapped_scan_gated_norm_stays_in_bounds(with_y, hb):
     """The overlapped form (head pairs, unsplit): its outputs and its ready queue (the
     workspace) stay inside their buffers, and the outputs equal the chained form's."""
-    s = _scan_case(64, H=16, G=1, seed=611)
+    s = _scan_case(64, H=16, G=1, seqs=SEQS + [2600], seed=611)   # >= 4096 tokens
     i = _scan_inputs(s)
     T, H, P, N, nseq = s.T, s.H, s.P, s.N, s.nseq
     nrm = I.make_norm_inputs(T, H * P, 256, act="bf16", seed=613)
     z, w = dev(nrm.z), dev(nrm.weight)
     kw = dict(cu_seqlens=i["cu"], chunk_size=128, group_size=256, eps=1e-5, D=i["D"],
               dt_bias=i["bias"], initial_states=i["init"], has_initial_state=i["hi"],
-              seg_chunks=-1, head_block=2)
+              seg_chunks=-1, head_block=hb, p_block=64)
     args = (i["x"], i["dt"], i["A"], i["B"], i["C"], z, w)
     chained = torch.empty(0, dtype=torch.uint8, device="cuda")
     out_ref, f_ref = ssd.chunk_scan_gated_norm(*args, workspace=chained, **kw)
@@ -138,7 +138,7 @@ def test_overlapped_scan_gated_norm_stays_in_bounds(with_y):
     y = Guarded((T, H, P), torch.bfloat16) if with_y else None
     nws = ssd.chunk_scan_gated_norm_workspace_size(
         i["x"], i["B"], i["C"], z, w, out.t, y=None if y is None else y.t, cu_seqlens=i["cu"],
-        chunk_size=128, group_size=256, seg_chunks=-1, head_block=2)
+        chunk_size=128, group_size=256, seg_chunks=-1, head_block=hb, p_block=64)
     assert nws > 0
     ws = Guarded((nws,), torch.uint8)
     st = Guarded((1,), torch.int32, fill=torch.zeros(1, dtype=torch.int32, device="cuda"))

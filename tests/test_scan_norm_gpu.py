@@ -70,13 +70,13 @@ def _fused(s, n, gs, *, want_y, seg_chunks=0, z=True, graph=False):
     return out, y, fs, bits
 
 
-def _separate(s, n, gs, *, seg_chunks=0, z=True, head_block=0):
+def _separate(s, n, gs, *, seg_chunks=0, z=True, head_block=0, p_block=0):
     d = _dev_inputs(s)
     y, fs = ssd.chunk_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=d["cu_seqlens"],
                            chunk_size=s.chunk_size, D=d["D"], dt_bias=d["dt_bias"],
                            initial_states=d["initial_states"],
                            has_initial_state=d["has_initial_state"], seg_chunks=seg_chunks,
-                           head_block=head_block)
+                           head_block=head_block, p_block=p_block)
     T, H, P = y.shape
     out = ssd.gated_rmsnorm(y.view(T, H * P), dev(n.z) if z else None, dev(n.weight),
                             group_size=gs, eps=n.eps)
@@ -251,28 +251,34 @@ def test_layer_mixed_nemotron_h_shapes_with_concurrent_decode():
 # The overlapped form: the scan (two heads per CTA, unsplit) appends each finished
 # 128-token chunk of each norm group to a queue in the workspace, and the norm, launched
 # as a programmatic dependent, normalises those rows while the scan runs on.  Each case is
-# checked to take that form (its workspace is the ready queue), then held bit for bit to
-# the chained form of the same call, to the two plain calls and to the oracle.
+# checked to take that form (its workspace is the ready queue; the form needs at least
+# 4096 tokens), then held bit for bit to the chained form of the same call, to the two
+# plain calls and to the oracle.
 OVERLAP_CASES = {
-    # ragged varlen with empty and one-token sequences: one group of 4 heads (2 CTAs)
+    # ragged varlen with empty and one-token sequences: one group of 4 heads
     "varlen_one_group_of_4_heads": (
-        lambda: I.make_scan_inputs([700, 129, 1, 0, 300, 1000, 257, 128, 385], H=4, P=64,
-                                   G=2, N=128, chunk_size=256, act="bf16", seed=211,
+        lambda: I.make_scan_inputs([700, 129, 1, 0, 300, 1000, 257, 128, 385, 1300], H=4,
+                                   P=64, G=2, N=128, chunk_size=256, act="bf16", seed=211,
                                    init="all"), 256),
-    # 16 heads in 4 groups of 4 heads: two CTAs per group, four groups per row
+    # 16 heads in 4 groups of 4 heads, four groups per row
     "groups_of_4_heads": (
-        lambda: I.make_scan_inputs([513, 64, 1300], H=16, P=64, G=2, N=128, chunk_size=128,
-                                   act="bf16", seed=213, init=[1, 0, 1]), 256),
-    # P = 128: each CTA's two 64-channel head blocks lie in two different groups
+        lambda: I.make_scan_inputs([513, 64, 1300, 2300], H=16, P=64, G=2, N=128,
+                                   chunk_size=128, act="bf16", seed=213, init=[1, 0, 1, 0]),
+        256),
+    # P = 128: a two-head CTA's two 64-channel head blocks lie in two different groups
     "p128_head_blocks_in_two_groups": (
-        lambda: I.make_scan_inputs([400, 777], H=4, P=128, G=1, N=128, chunk_size=128,
+        lambda: I.make_scan_inputs([400, 777, 3000], H=4, P=128, G=1, N=128, chunk_size=128,
                                    act="bf16", seed=215, init="all"), 256),
     # one group over all 1536 channels of the Mamba2-130M shape: 12 CTAs per group
     "mamba2_130m_one_group": (lambda: I.scan_workload("mamba2_130m"), 1536),
 }
 
 
-def _overlap_call(s, n, gs, *, workspace, want_y, z=True, status=None):
+# heads per CTA of the scan (both take the overlapped form, in 64-channel blocks)
+HB = [1, 2]
+
+
+def _overlap_call(s, n, gs, *, workspace, want_y, z=True, status=None, head_block=2):
     d = _dev_inputs(s)
     T, H, P = d["x"].shape
     zt, wt = (dev(n.z) if z else None), dev(n.weight)
@@ -285,8 +291,8 @@ def _overlap_call(s, n, gs, *, workspace, want_y, z=True, status=None):
                               group_size=gs, eps=n.eps, D=d["D"], dt_bias=d["dt_bias"],
                               initial_states=d["initial_states"],
                               has_initial_state=d["has_initial_state"], y=y, out=out,
-                              final_states=fs, status=status, seg_chunks=-1, head_block=2,
-                              workspace=workspace)
+                              final_states=fs, status=status, seg_chunks=-1,
+                              head_block=head_block, p_block=64, workspace=workspace)
     _, bits = ssd.read_status(status)
     return out, y, fs, bits
 
@@ -296,31 +302,33 @@ def _queue_bytes(s, d_channels, gs):
     return (nid * (d_channels // gs) * (4 + 4 * 8) + 16 + 255) // 256 * 256
 
 
-def _takes_overlapped_form(s, n, gs, z=True):
+def _takes_overlapped_form(s, n, gs, z=True, head_block=2):
     d = _dev_inputs(s)
     T, H, P = d["x"].shape
     out = torch.empty((T, H * P), dtype=d["x"].dtype, device="cuda")
     nws = ssd.chunk_scan_gated_norm_workspace_size(
         d["x"], d["B"], d["C"], dev(n.z) if z else None, dev(n.weight), out,
         cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size, group_size=gs, seg_chunks=-1,
-        head_block=2)
+        head_block=head_block, p_block=64)
     return nws == _queue_bytes(s, H * P, gs), nws
 
 
 @pytest.mark.parametrize("case", sorted(OVERLAP_CASES))
 @pytest.mark.parametrize("want_y", [True, False])
-def test_overlapped_scan_gated_norm(case, want_y):
+@pytest.mark.parametrize("hb", HB)
+def test_overlapped_scan_gated_norm(case, want_y, hb):
     make, gs = OVERLAP_CASES[case]
     s = make()
     n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=217)
-    ok, nws = _takes_overlapped_form(s, n, gs)
+    ok, nws = _takes_overlapped_form(s, n, gs, head_block=hb)
     assert ok, f"not the overlapped form (workspace {nws})"
-    out, y, fs, bits = _overlap_call(s, n, gs, workspace=None, want_y=want_y)
+    out, y, fs, bits = _overlap_call(s, n, gs, workspace=None, want_y=want_y, head_block=hb)
     assert bits == 0
     chained = torch.empty(0, dtype=torch.uint8, device="cuda")   # too small: the chained form
-    out_c, y_c, fs_c, bits_c = _overlap_call(s, n, gs, workspace=chained, want_y=want_y)
+    out_c, y_c, fs_c, bits_c = _overlap_call(s, n, gs, workspace=chained, want_y=want_y,
+                                             head_block=hb)
     assert bits_c == 0
-    out_sep, y_sep, fs_sep = _separate(s, n, gs, seg_chunks=-1, head_block=2)
+    out_sep, y_sep, fs_sep = _separate(s, n, gs, seg_chunks=-1, head_block=hb, p_block=64)
     assert torch.equal(out, out_c), "overlapped and chained forms differ"
     assert torch.equal(out, out_sep), "differs from the two plain calls"
     assert torch.equal(fs, fs_c) and torch.equal(fs, fs_sep)
@@ -380,23 +388,24 @@ def test_overlapped_no_gate_and_in_a_cuda_graph():
     assert bits == 0
 
 
-def test_overlapped_heads_with_A_not_negative():
+@pytest.mark.parametrize("hb", HB)
+def test_overlapped_heads_with_A_not_negative(hb):
     """Head pair 0 has both A >= 0 (its CTAs write zero rows and count every chunk at once),
     head 5 alone of its pair: the status bit is raised, the norm still receives every
     chunk, and the call equals its chained form bit for bit."""
-    s = I.make_scan_inputs([600, 37, 900], H=8, P=64, G=2, N=128, chunk_size=128,
+    s = I.make_scan_inputs([600, 37, 900, 2600], H=8, P=64, G=2, N=128, chunk_size=128,
                            act="bf16", seed=221, init="all")
     A = s.A.values.copy()
     A[0], A[1], A[5] = 0.0, np.nan, 0.5
     s.A = I.Tensor(A, "f32")
     gs = 256
     n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=223)
-    assert _takes_overlapped_form(s, n, gs)[0]
-    out, _, fs, bits = _overlap_call(s, n, gs, workspace=None, want_y=False)
+    assert _takes_overlapped_form(s, n, gs, head_block=hb)[0]
+    out, _, fs, bits = _overlap_call(s, n, gs, workspace=None, want_y=False, head_block=hb)
     assert bits & ssd.DEV_A_NOT_NEG
     out_c, _, fs_c, bits_c = _overlap_call(s, n, gs, workspace=torch.empty(0, dtype=torch.uint8,
                                                                             device="cuda"),
-                                           want_y=False)
+                                           want_y=False, head_block=hb)
     assert bits_c & ssd.DEV_A_NOT_NEG
     assert torch.equal(out, out_c)
     assert torch.equal(fs, fs_c)
