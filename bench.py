@@ -756,9 +756,15 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
         i = inputs(T)
         out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         fs = torch.empty((len(lens), H, P, N), dtype=torch.float32, device=dev)
-        nws = ssd.chunk_scan_workspace_size(i["x"], i["B"], i["C"], cu_seqlens=cu, chunk_size=128)
+        # the call's workspace: a split's, or the ready queue of its overlapped form
+        nws = ssd.chunk_scan_gated_norm_workspace_size(i["x"], i["B"], i["C"], i["z"], wn, out,
+                                                       cu_seqlens=cu, chunk_size=128,
+                                                       group_size=1024)
+        split = ssd.chunk_scan_workspace_size(i["x"], i["B"], i["C"], cu_seqlens=cu,
+                                              chunk_size=128)
         ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
-        return T, cu, i, out, fs, ws, nws > 0
+        form = "split" if split > 0 else ("overlapped" if nws > 0 else "chained")
+        return T, cu, i, out, fs, ws, form
 
     def timed_flushed(fn, n=iters):
         for _ in range(2):
@@ -776,10 +782,10 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
 
     single = {}
     for L in (1024, 4096, 16384, 65536):
-        T, cu, i, out, fs, ws, split = prepare([L])
+        T, cu, i, out, fs, ws, form = prepare([L])
         us = timed_flushed(lambda: layer_call(i, cu, 1, out, fs, ws))
         lb = layer_bytes(T, H, P, G, N, 1)
-        single[str(L)] = {"us": us, "tokens_per_s": T / (us / 1e6), "split_into_segments": split,
+        single[str(L)] = {"us": us, "tokens_per_s": T / (us / 1e6), "form": form,
                           "achieved_gbs": lb / (us / 1e6) / 1e9,
                           "frac_hbm": lb / (us / 1e6) / 1e9 / hbm_peak}
         del i, out, fs, ws
@@ -791,7 +797,7 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
 
     # mixed: 64 packed prefills + a 256-slot decode update on a second stream
     lens = np.random.default_rng(4243).integers(128, 4097, size=64)
-    T, cu, i, out, fs, ws, split = prepare(lens)
+    T, cu, i, out, fs, ws, form = prepare(lens)
     S = 256
     pool = torch.randn((S, H, P, N), generator=gen, device=dev)
     idx = torch.randperm(S, generator=gen, device=dev).to(torch.int32)
@@ -823,7 +829,7 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
                     "iterations",
         "wall_us": us_mixed, "tokens_per_s": (T + S) / (us_mixed / 1e6),
         "prefill_alone_us": us_prefill, "decode_alone_us": us_decode,
-        "split_into_segments": split,
+        "form": form,
         "achieved_gbs": (lb + ub) / (us_mixed / 1e6) / 1e9,
         "frac_hbm": (lb + ub) / (us_mixed / 1e6) / 1e9 / hbm_peak,
         "peak_kind": f"{peak_kind} hbm copy"}
