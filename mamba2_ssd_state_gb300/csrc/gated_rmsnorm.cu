@@ -152,12 +152,15 @@ __global__ void __launch_bounds__(256) norm_vec_kernel(const TA* x,
                                     part);
 }
 
-// The norm of the scan + norm call, fed by the scan's ready queue: each block takes the
-// next queue slot, waits (bounded) until the scan has appended a task there, and
-// normalises that task's rows of one group with the per-unit arithmetic of
-// norm_vec_kernel, so its outputs are bit for bit those of the standalone norm.  The
-// blocks start once every scan CTA has started (programmatic dependent launch), on SMs
-// the scan leaves free, and never wait for the scan grid itself.
+// The norm of the scan + norm call, fed by the scan's ready counters.  Tasks go in
+// chunk-major order — chunk 0 of every sequence, then chunk 1, ... — which follows the
+// order in which a scan grid finishes chunks; each is kReadyParts tasks of 32 rows per
+// norm group.  Each block takes the next task with an atomic, waits (bounded) until the
+// task's chunk-group counter is complete, and normalises the rows with the per-unit
+// arithmetic of norm_vec_kernel, so its outputs are bit for bit those of the standalone
+// norm.  The blocks start once every scan CTA has started (programmatic dependent
+// launch), on SMs the scan leaves free, and never wait for the scan grid itself until
+// their last task is done.
 template <typename TA, typename TW, int VPT, int TPG>
 __global__ void __launch_bounds__(256) norm_ready_kernel(const TA* x,
                                                          const TA* __restrict__ z,
@@ -169,49 +172,65 @@ __global__ void __launch_bounds__(256) norm_ready_kernel(const TA* x,
   constexpr int GPB = 256 / TPG;  // rows per block step
   constexpr int kRows = 128 / kReadyParts;
   __shared__ float part[8];
-  __shared__ long long red[8];
-  __shared__ unsigned long long task;
-  // the queue's length: every chunk of every sequence the scan accepts, once per group
-  long long mine = 0;
+  __shared__ int red[8];
+  __shared__ int task[3];  // sequence (-1: none left), chunk, part * ngroups + group
+  // the chunk-major task list spans max_s(chunks of s) chunk positions of nseq sequences
+  int mine = 0;
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
     const int t0 = cu[s], t1 = cu[s + 1];
-    if (0 <= t0 && t0 <= t1 && t1 <= T) mine += (t1 - t0 + 127) / 128;
+    if (0 <= t0 && t0 <= t1 && t1 <= T) mine = max(mine, (t1 - t0 + 127) / 128);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+  for (int off = 16; off > 0; off >>= 1) mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, off));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mine;
   __syncthreads();
-  long long total = 0;
-  for (int k = 0; k < 8; ++k) total += red[k];
-  total *= (long long)rq.ngroups * kReadyParts;
+  int maxc = 0;
+  for (int k = 0; k < 8; ++k) maxc = max(maxc, red[k]);
+  const int per_pos = rq.ngroups * kReadyParts;  // tasks per (chunk, sequence)
+  const long long total = (long long)maxc * nseq * per_pos;
   for (;;) {
     if (threadIdx.x == 0) {
-      unsigned long long v = 0;
-      const long long idx = atomicAdd(rq.head, 1);
-      if (idx < total) {
-        const volatile unsigned long long* slot = rq.q + idx;
+      int ts = -1, tc = 0, tk = 0;
+      for (;;) {  // the next task of a chunk that exists
+        const long long idx = atomicAdd(rq.head, 1);
+        if (idx >= total) break;
+        const long long pos = idx / per_pos;
+        const int c = (int)(pos / nseq), s = (int)(pos % nseq);
+        const int t0 = cu[s], t1 = cu[s + 1];
+        if (!(0 <= t0 && t0 <= t1 && t1 <= T) || c >= (t1 - t0 + 127) / 128) continue;
+        ts = s;
+        tc = c;
+        tk = (int)(idx % per_pos);
+        // wait until every output warp of the scan has counted this chunk-group
+        const int grp = tk % rq.ngroups;
+        const long long id = (long long)(t0 / 128) + s + c;
+        const volatile int* cnt = rq.cnt + id * rq.ngroups + grp;
         const long long t_start = clock64();
-        while ((v = *slot) == 0ull) {
-          if (*(volatile int*)rq.abort) break;
+        while (*cnt < rq.target) {
+          if (*(volatile int*)rq.abort) {
+            ts = -1;
+            break;
+          }
           if (clock64() - t_start > SSD_WAIT_LIMIT_CYCLES) {
             atomicExch(rq.abort, 1);
             set_status(status, SSD_DEV_TIMEOUT);
+            ts = -1;
             break;
           }
           __nanosleep(128);
         }
-        __threadfence();  // the task's rows of y are visible from here on
+        __threadfence();  // the rows the counter stands for are visible from here on
+        break;
       }
-      task = v;
+      task[0] = ts;
+      task[1] = tc;
+      task[2] = tk;
     }
     __syncthreads();
-    const unsigned long long v = task;
+    const int s = task[0], c = task[1], tk = task[2];
     __syncthreads();
-    if (v == 0ull) break;
-    const int s = (int)(v >> 32) - 1;
-    const int c = (int)((v >> 15) & 0x1ffffu);
-    const int k = (int)((v >> 12) & 7u);
-    const int grp = (int)(v & 0xfffu);
+    if (s < 0) break;
+    const int grp = tk % rq.ngroups, k = tk / rq.ngroups;
     const int t1 = cu[s + 1];
     const int r0 = cu[s] + 128 * c + kRows * k;
     const int r1 = min(t1, r0 + kRows);
@@ -375,25 +394,17 @@ cudaError_t launch_norm_ready(const void* x, const void* z, const void* w, void*
 
 size_t ready_queue_bytes(int64_t T, int nseq, int ngroups) {
   const int64_t nid = (T + 127) / 128 + nseq;
-  const size_t ntask = (size_t)nid * ngroups;
-  const size_t bytes = ntask * sizeof(int) + ntask * kReadyParts * sizeof(unsigned long long) +
-                       4 * sizeof(int);
+  const size_t bytes = (size_t)nid * ngroups * sizeof(int) + 4 * sizeof(int);
   return (bytes + 255) / 256 * 256;
 }
 
 ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs) {
   const int64_t nid = (T + 127) / 128 + nseq;
-  const size_t ntask = (size_t)nid * ngroups;
-  char* p = static_cast<char*>(ws);
+  int* p = static_cast<int*>(ws);
   ReadyQueue rq;
-  // the 8-byte task slots first (the workspace is 256-byte aligned), then the counters
-  rq.q = reinterpret_cast<unsigned long long*>(p);
-  p += ntask * kReadyParts * sizeof(unsigned long long);
-  rq.cnt = reinterpret_cast<int*>(p);
-  p += ntask * sizeof(int);
-  rq.head = reinterpret_cast<int*>(p);
-  rq.tail = rq.head + 1;
-  rq.abort = rq.head + 2;
+  rq.cnt = p;
+  rq.head = p + (size_t)nid * ngroups;
+  rq.abort = rq.head + 1;
   rq.nid = nid;
   rq.ngroups = ngroups;
   rq.gs = gs;

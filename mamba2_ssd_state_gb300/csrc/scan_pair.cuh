@@ -45,10 +45,7 @@ constexpr int kPairMaskWarps = 8, kPairStateWarps = 4, kPairEpiWarps = 4;
 constexpr int kDecay0 = 2, kMask0 = 4, kState0 = kMask0 + kPairMaskWarps;
 constexpr int kEpi0 = kState0 + kPairStateWarps;
 constexpr int kPairThreads = 32 * (kEpi0 + kPairEpiWarps);
-// the scan of the scan + norm call adds one warp, the ready-queue publisher (its own
-// instantiation: with 21 warps the register budget per thread drops from 96 to 80)
-constexpr int kPub = kEpi0 + kPairEpiWarps;
-template <bool kReady> constexpr int pair_threads() { return kPairThreads + (kReady ? 32 : 0); }
+template <bool kReady> constexpr int pair_threads() { return kPairThreads; }
 constexpr int kTile = 16384;            // one head's [128 rows][64] bf16 tile
 constexpr int kB = 0;                   // B tile, two 64-wide 128B-swizzled boxes
 constexpr int kC = 32768;               // C tile
@@ -57,7 +54,7 @@ constexpr int kXs = kX + 4 * kTile;     // w o x, 2 heads
 constexpr int kHT = kXs + 2 * kTile;    // h^T bf16, 2 heads: [n rows][64 p]
 constexpr int kPro = kHT + 2 * kTile;   // float [NB][2][kProStride]
 constexpr int kBar = kPro + NB * 2 * kProStride * 4;
-constexpr int kNumBar = 2 * 2 + 2 + 2 + 2 * NB + 11;
+constexpr int kNumBar = 2 * 2 + 2 + 2 + 2 * NB + 10;
 constexpr int kFlags = kBar + kNumBar * 8;
 constexpr int kSmemBytes = kFlags + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
@@ -146,10 +143,10 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
   // every thread whose y stores they stand for)
   auto publish = [&](int cc, int per) {
     if (grp0 == grp1) {
-      ready_publish(prm.rq, id0 + cc, s, cc, grp0, 2 * per);
+      ready_count(prm.rq, id0 + cc, grp0, 2 * per);
     } else {
-      ready_publish(prm.rq, id0 + cc, s, cc, grp0, per);
-      ready_publish(prm.rq, id0 + cc, s, cc, grp1, per);
+      ready_count(prm.rq, id0 + cc, grp0, per);
+      ready_count(prm.rq, id0 + cc, grp1, per);
     }
   };
   if (bad0 && bad1) {
@@ -185,8 +182,7 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
   uint64_t* h_ready = cb_full + 6;       //      scaled state in TMEM, h^T in smem (4 state)
   uint64_t* y_empty = cb_full + 7;       //      Y and Yoff read (4 epilogue warps)
   uint64_t* drain = cb_full + 8;         //      teardown: all MMAs retired
-  uint64_t* pub_done = cb_full + 9;      //      scan + norm call: chunk published
-  static_assert(kNumBar == 8 + 2 * NB + 11, "barrier block size");
+  static_assert(kNumBar == 8 + 2 * NB + 10, "barrier block size");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kFlags + 4);
 
@@ -212,7 +208,6 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     mbar_init(h_ready, kPairStateWarps);
     mbar_init(y_empty, kPairEpiWarps);
     mbar_init(drain, 1);
-    mbar_init(pub_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     // thread 0 is the TMA producer: chunk 0's tiles (and chunk 1's x) are on their way
@@ -324,31 +319,6 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
       if (nc > 0) mbar_wait_drain(c_full, (nc - 1) & 1, kWaitLimit);
       for (int c = nx > 2 ? nx - 2 : 0; c < nx; ++c)
         mbar_wait_drain(&x_full[c & 1], (c >> 1) & 1, kWaitLimit);
-    }
-  } else if (kReady && warp == kPub) {
-    if (lane == 0 && ready) {
-      // the publisher of the scan + norm call: once the four output warps have written
-      // chunk cc (their y_empty arrivals release their stores to this CTA), make those
-      // rows visible to the whole GPU, count them in the norm's ready queue and tell the
-      // output warps (who wait for it before they finish chunk cc + 1, so y_empty is never
-      // two phases ahead of this loop).  The atomics' round trips stay off the output
-      // warps; the barrier is polled with sleeps, the cheapest way to watch it.
-      for (int cc = 0; cc < nch; ++cc) {
-        const long long t0 = clock64();
-        bool ok = true;
-        while (!mbar_test_wait(y_empty, cc & 1)) {
-          if (*abort_flag || clock64() - t0 > kWaitLimit) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          __nanosleep(256);
-        }
-        if (!ok) break;
-        __threadfence();
-        publish(cc, kPairEpiWarps);
-        mbar_arrive(pub_done);
-      }
     }
   } else if (warp >= kDecay0 && warp < kMask0) {
     // ------------------------------------------------------------ decay warps (one per head)
@@ -741,12 +711,22 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
     const float D0 = prm.D ? prm.D[h0] : 0.f, D1 = prm.D ? prm.D[h0 + 1] : 0.f;
     const bool wide = ((uintptr_t)prm.y & 31u) == 0;  // 32-byte stores need 32-byte rows
-    for (int c = 0; c < nch; ++c) {
+    // the scan + norm call: this warp's rows of chunk cc are written; make them visible
+    // to the whole GPU and count them (one contribution per head block).  Done one chunk
+    // late, when the stores have long landed, so the fence waits for little.
+    auto release_rows = [&](int cc) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) publish(cc, 1);
+    };
+    int c = 0;
+    for (; c < nch; ++c) {
       const int b = c % NB, sx = c & 1;
       if (!wwait(y_full, c & 1)) break;
       if (!wwait(o_full, c & 1)) break;
       if (!wwait(&x_full[sx], (c >> 1) & 1)) break;
       if (!wwait(&pro_full[b], (c / NB) & 1)) break;
+      if (ready && c > 0) release_rows(c - 1);
       tc_fence_after();
       const int tok = tb + c * QT + r;
 #pragma unroll 1
@@ -786,8 +766,6 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
         }
       }
       tc_fence_before();
-      // chunk c - 1 is published, so the publisher has seen y_empty's previous phase
-      if (ready && c >= 1 && !wwait(pub_done, (c - 1) & 1)) break;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(y_empty);
@@ -795,6 +773,7 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
         mbar_arrive(&pro_empty[b]);
       }
     }
+    if (ready && c == nch && nch > 0) release_rows(nch - 1);
   }
 
   __syncthreads();

@@ -76,10 +76,7 @@ constexpr int NB = 3;            // depth of the decay buffer ring
 constexpr int kMaskWarps = 8, kOutWarps = 4;
 constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
 constexpr int kThreads = 32 * (kDecayWarp + 1);
-// the scan of the scan + norm call (kReady) adds warp kDecayWarp + 1, the ready-queue
-// publisher; with 16 warps the register budget per thread stays at 128
-constexpr int kPubWarp = kDecayWarp + 1;
-template <bool kReady> constexpr int tc_threads() { return kThreads + (kReady ? 32 : 0); }
+template <bool kReady> constexpr int tc_threads() { return kThreads; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFactorLimit = 64.f;            // log2 bound of a factorised decay factor
 constexpr long long kWaitLimit = SSD_WAIT_LIMIT_CYCLES;  // SM cycles a wait may take
@@ -135,7 +132,7 @@ struct Layout {
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
   static constexpr int kPro = kHT + 2 * kHTPad;        // float [NB][kProStride]
   static constexpr int kBar = kPro + NB * kProStride * 4;
-  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 13 + 3 * NXS;
+  static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS;
   static constexpr int kFlags = kBar + kNumBar * 8;    // abort flag, TMEM base
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
@@ -240,8 +237,7 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0)
-        for (int cc = 0; cc < nch; ++cc)
-          ready_publish(prm.rq, id0 + cc, s, cc, grp, kOutWarps);
+        for (int cc = 0; cc < nch; ++cc) ready_count(prm.rq, id0 + cc, grp, kOutWarps);
     }
     return;
   }
@@ -269,8 +265,7 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
   uint64_t* yoff_full = h_ready + 2;        // [2]   Yoff buffer done
   uint64_t* y_empty = yoff_full + 2;        // [2]   Y and Yoff buffers read (4 output warps)
   uint64_t* drain = y_empty + 2;            //       teardown: all MMAs retired
-  uint64_t* pub_done = drain + 1;           //       scan + norm call: chunk published
-  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 13 + 3 * NXS,
+  static_assert(L::kNumBar == 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS,
                 "barrier block size must match the barriers laid out here");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kFlags + 4);
@@ -307,7 +302,6 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
       mbar_init(&y_empty[i], kOutWarps);
     }
     mbar_init(drain, 1);
-    mbar_init(pub_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     // thread 0 is the TMA producer: chunk 0's tiles are on their way while the rest of
@@ -402,30 +396,6 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
         mbar_wait_drain(&c_full[c % NBC], (c / NBC) & 1, kWaitLimit);
       for (int c = nx_iss > NX ? nx_iss - NX : 0; c < nx_iss; ++c)
         mbar_wait_drain(&x_full[c % NX], (c / NX) & 1, kWaitLimit);
-    }
-  } else if (kReady && warp == kPubWarp) {
-    if (lane == 0 && ready) {
-      // the publisher of the scan + norm call: once the four output warps have written
-      // chunk cc (their y_empty arrivals release their stores to this CTA), make those
-      // rows visible to the whole GPU, count them in the norm's ready queue and tell the
-      // output warps, who wait for it before they finish chunk cc + 1 (so y_empty of a
-      // buffer is never a phase ahead of this loop)
-      for (int cc = 0; cc < nch; ++cc) {
-        const long long t_wait = clock64();
-        bool ok = true;
-        while (!mbar_test_wait(&y_empty[cc & 1], (cc >> 1) & 1)) {
-          if (*abort_flag || clock64() - t_wait > kWaitLimit) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          __nanosleep(256);
-        }
-        if (!ok) break;
-        __threadfence();
-        ready_publish(prm.rq, id0 + cc, s, cc, grp, kOutWarps);
-        mbar_arrive(pub_done);
-      }
     }
   } else if (warp == kDecayWarp) {
     // ------------------------------------------------------------ decay warp
@@ -740,8 +710,16 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
     };
     write_hT(1);
     const float Dh = prm.D ? prm.D[h] : 0.f;
+    // the scan + norm call: this warp's rows of chunk cc are written; make them visible to
+    // the whole GPU and count them.  Done one chunk late, when the stores have long landed.
+    auto release_rows = [&](int cc) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) ready_count(prm.rq, id0 + cc, grp, 1);
+    };
     bool ok = true;
-    for (int c = 0; c < nch; ++c) {
+    int c = 0;
+    for (; c < nch; ++c) {
       const int b = c % NB, sx = c % NX;
       if (!(ok = wwait(&pro_full[b], (c / NB) & 1))) break;
       if (!(ok = wwait(&s_full[c % NXS], (c / NXS) & 1))) break;
@@ -766,6 +744,7 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
       if (!(ok = wwait(&y_full[c & 1], (c >> 1) & 1))) break;
       if (!(ok = wwait(&yoff_full[c & 1], (c >> 1) & 1))) break;
       if (!(ok = wwait(&x_full[sx], (c / NX) & 1))) break;
+      if (ready && c > 0) release_rows(c - 1);
       tc_fence_after();
       const float e_i = ex2(pb[kProCs + r]);
       const int tok = tb + c * QT + r;
@@ -797,8 +776,6 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
         }
       }
       tc_fence_before();
-      // chunk c - 1 is published, so the publisher has seen y_empty's previous phase
-      if (ready && c >= 1 && !(ok = wwait(pub_done, (c - 1) & 1))) break;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&y_empty[c & 1]);
@@ -806,6 +783,7 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
         mbar_arrive(&pro_empty[b]);
       }
     }
+    if (ready && c == nch && nch > 0) release_rows(nch - 1);
     // the final state, or a segment's local end state (the fix-up kernel chains those)
     float* hout = ok ? end_state() : nullptr;
     if (hout) {

@@ -37,46 +37,35 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bit) {
 
 // Hand-off of finished rows of y from the scan to the gated norm of the scan + norm call,
 // so that the norm runs while the scan still works on later chunks.  For every 128-token
-// chunk of every sequence and every norm group, the scan's output warps count what they
-// have written (each warp: its 32 rows of one 64-channel head block); the warp whose
-// count completes the chunk-group appends it, as kReadyParts tasks of 32 rows, to a
-// queue, which the norm kernel drains in completion order.
+// chunk of every sequence and every norm group there is a counter: each output warp of
+// the scan, once its 32 rows of one 64-channel head block of a chunk are written and
+// fenced, adds one to it (a reduction nobody waits for), so a chunk-group is complete
+// when its counter reaches 4 per 64-channel block of the group.  The norm kernel takes
+// chunk-groups in chunk-major order (chunk 0 of every sequence, then chunk 1, ...), as
+// kReadyParts tasks of 32 rows, and polls each one's counter before it reads the rows.
 // Chunk ids: chunk c of sequence s (tokens from t0 = cu_seqlens[s]) is floor(t0 / 128) +
 // s + c, distinct for nondecreasing cu_seqlens and below ceil(T / 128) + nseq.
 constexpr int kReadyParts = 4;
 struct ReadyQueue {
-  int* cnt;                // [nid * ngroups] contributions so far (zeroed before the call)
-  unsigned long long* q;   // [nid * ngroups * kReadyParts] tasks; 0 = not yet appended
-  int* head;               // next queue slot a norm block takes
-  int* tail;               // next free queue slot
-  int* abort;              // set when a wait gave up: every later wait gives up at once
-  long long nid;           // chunk ids: ceil(T / 128) + nseq
-  int ngroups;             // norm groups per row
-  int gs;                  // channels per norm group
-  int target;              // contributions that complete a chunk-group: 4 per 64 channels
+  int* cnt;       // [nid * ngroups] contributions so far (zeroed before the call)
+  int* head;      // next task a norm block takes
+  int* abort;     // set when a wait gave up: every later wait gives up at once
+  long long nid;  // chunk ids: ceil(T / 128) + nseq
+  int ngroups;    // norm groups per row
+  int gs;         // channels per norm group
+  int target;     // contributions that complete a chunk-group: 4 per 64 channels
 };
-// Task word: (s + 1) << 32 | c << 15 | part << 12 | group.
-__host__ __device__ constexpr unsigned long long ready_task(int s, int c, int part, int grp) {
-  return ((unsigned long long)(s + 1) << 32) | ((unsigned long long)c << 15) |
-         ((unsigned long long)part << 12) | (unsigned long long)grp;
-}
-static_assert(kReadyParts <= 8 && 128 % kReadyParts == 0, "part field: 3 bits");
-constexpr int kReadyMaxGroups = 4096;           // group field: 12 bits
-constexpr long long kReadyMaxChunks = 1 << 17;  // chunk field: 17 bits
-// Count inc contributions to (chunk id, group); the one that completes it appends the
-// chunk-group's tasks.  Call after a __threadfence() of every thread whose stores it
-// stands for (and a warp or block barrier between those threads and the caller).
-__device__ __forceinline__ void ready_publish(const ReadyQueue& rq, long long id, int s, int c,
-                                              int grp, int inc) {
+static_assert(128 % kReadyParts == 0, "tasks of whole rows");
+// Count inc contributions to (chunk id, group).  Call after a __threadfence() of every
+// thread whose stores they stand for (and a warp or block barrier between those threads
+// and the caller).
+__device__ __forceinline__ void ready_count(const ReadyQueue& rq, long long id, int grp,
+                                            int inc) {
   if (id < 0 || id >= rq.nid) return;  // only for cu_seqlens that are not nondecreasing
-  const int old = atomicAdd(rq.cnt + id * rq.ngroups + grp, inc);
-  if (old + inc != rq.target) return;
-  __threadfence();
-  const int pos = atomicAdd(rq.tail, kReadyParts);
-  for (int k = 0; k < kReadyParts; ++k) atomicExch(rq.q + pos + k, ready_task(s, c, k, grp));
+  atomicAdd(rq.cnt + id * rq.ngroups + grp, inc);  // result unused: a reduction
 }
-// Workspace of the queue for T tokens in nseq sequences (256-byte multiple; zero it
-// before each call), and the queue laid out at ws.
+// Workspace of the counters for T tokens in nseq sequences (256-byte multiple; zero it
+// before each call), and the counters laid out at ws.
 size_t ready_queue_bytes(int64_t T, int nseq, int ngroups);
 ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs);
 
@@ -88,8 +77,8 @@ cudaError_t launch_gated_rmsnorm(const void* x, const void* z, const void* w, vo
                                  int64_t rows, int d, int gs, float eps, ssd_dtype act,
                                  ssd_dtype wt, cudaStream_t s, bool pdl = false);
 cudaError_t launch_scan_simt(const ssd_scan_args& a, cudaStream_t s);
-// The gated norm that drains a ReadyQueue (launched as a programmatic dependent of the
-// scan that fills it; it does not wait for the scan's completion).  False when this
+// The gated norm that follows a ReadyQueue's counters (launched as a programmatic
+// dependent of the scan that fills them; it does not wait for the scan's completion).  False when this
 // activation / weight type, group size or alignment has no such kernel.
 bool norm_ready_supported(const void* x, const void* z, const void* w, const void* out, int d,
                           int gs, ssd_dtype act);

@@ -145,9 +145,8 @@ def test_scan_workspace_size(lib):
 def test_scan_gated_norm_workspace_size(lib):
     """Host-side planning only: no kernel runs.  The overlapped scan + norm (two heads per
     CTA, unsplit, bf16, groups of whole 64-channel head blocks, 16-byte aligned rows, at
-    most two waves of CTAs) wants its ready queue: per chunk id (ceil(T/128) + nseq of
-    them) and norm group, one int count and four 8-byte task slots, plus four ints,
-    rounded up to 256 bytes (norm groups the vector norm takes: 8 x 32 x v channels, v
+    most two waves of CTAs) wants its ready counters: one int per chunk id (ceil(T/128) +
+    nseq of them) and norm group, plus four ints, rounded up to 256 bytes (norm groups the vector norm takes: 8 x 32 x v channels, v
     <= 4, and multiples).  A split the planner would choose takes the workspace
     instead; anything the overlapped form cannot take (or fewer than 4096 tokens) wants
     none."""
@@ -157,8 +156,7 @@ def test_scan_gated_norm_workspace_size(lib):
     lib.ssd_chunk_scan_gated_norm_workspace_size.restype = ctypes.c_size_t
     kw = dict(act_dtype=ssd.SSD_BF16, nseq=4, T=16384, H=128, P=64, G=8, N=128, chunk_size=128)
     r256 = lambda b: (b + 255) // 256 * 256
-    queue = lambda T, nseq, ngroups: r256(((T + 127) // 128 + nseq) * ngroups * (4 + 4 * 8)
-                                          + 16)
+    queue = lambda T, nseq, ngroups: r256(((T + 127) // 128 + nseq) * ngroups * 4 + 16)
 
     def size(gs=1024, z=0x200000, w=0x300000, out=0x400000, y=0x100000, **o):
         a = _scan_args(**{**kw, **o})

@@ -248,12 +248,12 @@ def test_layer_mixed_nemotron_h_shapes_with_concurrent_decode():
     check_bf16("mixed decode pool", pool.cpu().numpy(), ref_pool)
 
 
-# The overlapped form: the scan (two heads per CTA, unsplit) appends each finished
-# 128-token chunk of each norm group to a queue in the workspace, and the norm, launched
-# as a programmatic dependent, normalises those rows while the scan runs on.  Each case is
-# checked to take that form (its workspace is the ready queue; the form needs at least
-# 4096 tokens), then held bit for bit to the chained form of the same call, to the two
-# plain calls and to the oracle.
+# The overlapped form: the scan (unsplit, 64-channel blocks) counts each finished 128-token
+# chunk of each norm group in the workspace, and the norm, launched as a programmatic
+# dependent, normalises those rows while the scan runs on.  Each case is checked to take
+# that form (its workspace is the ready counters; the form needs at least 4096 tokens),
+# then held bit for bit to the chained form of the same call, to the two plain calls and
+# to the oracle.
 OVERLAP_CASES = {
     # ragged varlen with empty and one-token sequences: one group of 4 heads
     "varlen_one_group_of_4_heads": (
@@ -299,7 +299,7 @@ def _overlap_call(s, n, gs, *, workspace, want_y, z=True, status=None, head_bloc
 
 def _queue_bytes(s, d_channels, gs):
     nid = -(-s.T // 128) + s.nseq
-    return (nid * (d_channels // gs) * (4 + 4 * 8) + 16 + 255) // 256 * 256
+    return (nid * (d_channels // gs) * 4 + 16 + 255) // 256 * 256
 
 
 def _takes_overlapped_form(s, n, gs, z=True, head_block=2):
