@@ -257,7 +257,7 @@ def run_ours(args, rank, world, local_rank):
         ssd.state_update(pool, uidx, i["ux"], i["udt"], A, i["uB"], i["uC"], D=Dp, dt_bias=bias,
                          y=uy, status=status, stream=st)
 
-    # the call's workspace: the ready queue of its overlapped form (the norm normalises the
+    # the call's workspace: the ready counters of its overlapped form (the norm normalises the
     # scan's finished chunks while the scan runs), or a split's, or none
     lws_bytes = ssd.chunk_scan_gated_norm_workspace_size(x, B, C, z, wt, out, cu_seqlens=cu,
                                                          chunk_size=s.chunk_size,
@@ -457,8 +457,8 @@ def run_ours(args, rank, world, local_rank):
                              "gated norm in one call (the norm a programmatic dependent of the "
                              "scan), then the decode token",
                    "norm_form": norm_form + (
-                       ": the scan appends each finished 128-token chunk of each norm group "
-                       "to a queue and the norm kernel normalises those rows while the scan "
+                       ": the scan counts each finished 128-token chunk of each norm group "
+                       "and the norm kernel normalises those rows while the scan "
                        "runs" if norm_form == "overlapped" else ": the norm follows the scan"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "breakdown_us": {"scan": 1e3 * med(scan_ms), "gated_rmsnorm": 1e3 * med(norm_ms),
@@ -753,7 +753,7 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
         i = inputs(T)
         out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         fs = torch.empty((len(lens), H, P, N), dtype=torch.float32, device=dev)
-        # the call's workspace: a split's, or the ready queue of its overlapped form
+        # the call's workspace: a split's, or the ready counters of its overlapped form
         nws = ssd.chunk_scan_gated_norm_workspace_size(i["x"], i["B"], i["C"], i["z"], wn, out,
                                                        cu_seqlens=cu, chunk_size=128,
                                                        group_size=1024)

@@ -211,11 +211,11 @@ SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_strea
  *     two waves of CTAs (bf16, T >= 4096, group_size a multiple of 64 that the vector
  *     norm takes, 16-byte aligned rows) and args->workspace holds at least
  *     ssd_chunk_scan_gated_norm_workspace_size bytes (256-byte aligned; the call zeroes
- *     the bytes it uses, with a memset on the stream), the scan appends every finished
- *     128-token chunk of every norm group to a queue in the workspace, and the norm,
- *     launched as a programmatic dependent of the scan, normalises those rows while the
- *     scan works on later chunks.  Each wait of the norm on the queue is bounded (about
- *     2 s; SSD_DEV_TIMEOUT in d_status when one gives up, as when the scan aborts).
+ *     the bytes it uses, with a memset on the stream), the scan counts every finished
+ *     128-token chunk of every norm group in the workspace, and the norm, launched as a
+ *     programmatic dependent of the scan, normalises those rows while the scan works on
+ *     later chunks.  Each wait of the norm on a count is bounded (about 2 s;
+ *     SSD_DEV_TIMEOUT in d_status when one gives up, as when the scan aborts).
  *   - chained: otherwise the norm follows the scan, also as a programmatic dependent: its
  *     blocks take the SMs the scan leaves idle and load z and the weights while the scan
  *     runs, then wait for the scan to complete (griddepcontrol.wait) before they read y.
@@ -240,8 +240,8 @@ SSD_API ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const vo
 /* ------------------------------------------------------------------------------------
  * ssd_chunk_scan_gated_norm_workspace_size -- device workspace (bytes) that
  * ssd_chunk_scan_gated_norm wants for these arguments: the split of the scan when its
- * planner would split (ssd_chunk_scan_workspace_size), else the ready queue of the
- * overlapped form (about 12 bytes per 128-token chunk and norm group), else 0.  Reads
+ * planner would split (ssd_chunk_scan_workspace_size), else the ready counters of the
+ * overlapped form (4 bytes per 128-token chunk and norm group), else 0.  Reads
  * only shapes, pointers' alignment and the plan inputs of args (no device memory);
  * invalid arguments give 0.  The library does not name a counterpart of this split of
  * the scan + norm call in the source pages: it exists so that the norm may run while the

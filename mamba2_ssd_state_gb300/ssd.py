@@ -209,7 +209,7 @@ def chunk_scan_gated_norm(x, dt, A, B, C, z, norm_weight, *, cu_seqlens, chunk_s
         return_final_states, status, impl, p_block, seg_chunks, workspace, head_block,
         alloc_ws=False)
     if workspace is None:
-        # the split of the scan, or the ready queue of the overlapped form
+        # the split of the scan, or the ready counters of the overlapped form
         nbytes = lib.ssd_chunk_scan_gated_norm_workspace_size(
             ctypes.byref(a), _ptr(z), _ptr(norm_weight), int(group_size), _ptr(out))
         if nbytes:
@@ -305,7 +305,7 @@ def chunk_scan_gated_norm_workspace_size(x, B, C, z, norm_weight, out, *, cu_seq
                                          p_block=0, seg_chunks=0, head_block=0):
     """Bytes of workspace chunk_scan_gated_norm wants for these tensors
     (ssd_chunk_scan_gated_norm_workspace_size in ssd.h): the split of the scan when its
-    planner splits, else the ready queue of the overlapped form, else 0."""
+    planner splits, else the ready counters of the overlapped form, else 0."""
     lib = load_library()
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
