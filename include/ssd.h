@@ -208,7 +208,7 @@ SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_strea
  *
  * Two forms, the same results bit for bit:
  *   - overlapped: when the tensor-core scan runs unsplit in 64-channel blocks with at most
- *     two waves of CTAs (bf16, T >= 4096, group_size a multiple of 64 that the vector
+ *     two waves of CTAs (bf16, T >= 3072, group_size a multiple of 64 that the vector
  *     norm takes, 16-byte aligned rows) and args->workspace holds at least
  *     ssd_chunk_scan_gated_norm_workspace_size bytes (256-byte aligned; the call zeroes
  *     the bytes it uses, with a memset on the stream), the scan counts every finished

@@ -51,10 +51,11 @@ ssd_status validate_update(const ssd_update_args* a) {
 
 // Workspace of the overlapped scan + norm (0 = the call runs the norm after the scan):
 // the tensor-core scan unsplit in 64-channel blocks, bf16, a norm group of whole blocks,
-// a norm kernel for this group size and alignment, and enough tokens: below 4096 the
-// norm is short and the queue's fixed costs (its memset, the norm grid's tail) outweigh
-// the overlap (measured on one 1024-token Nemotron-H sequence: 54 us against 42 us).
-constexpr int32_t kReadyMinTokens = 4096;
+// a norm kernel for this group size and alignment, and enough tokens: on short inputs
+// the norm is short and the fixed costs (the counters' memset, the norm grid's tail)
+// outweigh the overlap (one Nemotron-H sequence: 50 against 42 us at 1024 tokens, 73
+// against 71 at 2048, 93 against 102 at 3072).
+constexpr int32_t kReadyMinTokens = 3072;
 
 size_t gated_norm_ready_bytes(const ssd_scan_args& a, const void* z, const void* w,
                               int32_t group_size, const void* out) {

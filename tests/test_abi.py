@@ -148,7 +148,7 @@ def test_scan_gated_norm_workspace_size(lib):
     most two waves of CTAs) wants its ready counters: one int per chunk id (ceil(T/128) +
     nseq of them) and norm group, plus four ints, rounded up to 256 bytes (norm groups the vector norm takes: 8 x 32 x v channels, v
     <= 4, and multiples).  A split the planner would choose takes the workspace
-    instead; anything the overlapped form cannot take (or fewer than 4096 tokens) wants
+    instead; anything the overlapped form cannot take (or fewer than 3072 tokens) wants
     none."""
     lib.ssd_chunk_scan_gated_norm_workspace_size.argtypes = [
         ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
@@ -188,8 +188,8 @@ def test_scan_gated_norm_workspace_size(lib):
     assert size(act_dtype=ssd.SSD_F32) == 0              # fp32: no tensor-core scan
     assert size(nseq=8, T=32768) == 0                    # 512 CTAs: more than two waves
     assert size(T=0) == 0
-    assert size(nseq=1, T=4095) == 0                     # short: the norm follows the scan
-    assert size(nseq=1, T=4096) == queue(4096, 1, 8)
+    assert size(nseq=1, T=3071) == 0                     # short: the norm follows the scan
+    assert size(nseq=1, T=3072) == queue(3072, 1, 8)
     assert size(gs=0) == 0 and size(gs=1000) == 0        # invalid group sizes
     # a split the planner is told to make takes the workspace (the norm then follows)
     split = lib.ssd_chunk_scan_workspace_size(ctypes.byref(_scan_args(**kw, seg_chunks=4)))

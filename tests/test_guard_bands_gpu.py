@@ -122,7 +122,7 @@ def test_scan_gated_norm_outputs_stay_in_bounds(with_y):
 def test_overlapped_scan_gated_norm_stays_in_bounds(with_y, hb):
     """The overlapped form (head pairs, unsplit): its outputs and its ready queue (the
     workspace) stay inside their buffers, and the outputs equal the chained form's."""
-    s = _scan_case(64, H=16, G=1, seqs=SEQS + [2600], seed=611)   # >= 4096 tokens
+    s = _scan_case(64, H=16, G=1, seqs=SEQS + [2600], seed=611)   # >= 3072 tokens
     i = _scan_inputs(s)
     T, H, P, N, nseq = s.T, s.H, s.P, s.N, s.nseq
     nrm = I.make_norm_inputs(T, H * P, 256, act="bf16", seed=613)

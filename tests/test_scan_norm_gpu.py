@@ -251,7 +251,7 @@ def test_layer_mixed_nemotron_h_shapes_with_concurrent_decode():
 # The overlapped form: the scan (unsplit, 64-channel blocks) counts each finished 128-token
 # chunk of each norm group in the workspace, and the norm, launched as a programmatic
 # dependent, normalises those rows while the scan runs on.  Each case is checked to take
-# that form (its workspace is the ready counters; the form needs at least 4096 tokens),
+# that form (its workspace is the ready counters; the form needs at least 3072 tokens),
 # then held bit for bit to the chained form of the same call, to the two plain calls and
 # to the oracle.
 OVERLAP_CASES = {

@@ -117,7 +117,7 @@ def test_overlapped_norm_stops_waiting_when_the_scan_aborts(fault_lib, hb):
     flag, the norm's blocks stop waiting for the chunks that will not come, and the call
     ends with SSD_DEV_TIMEOUT on a context that still runs the regular library."""
     # 4 heads (two head pairs), one norm group over their 256 channels; 4200 tokens (the
-    # overlapped form needs at least 4096)
+    # overlapped form needs at least 3072)
     s = I.make_scan_inputs([4200], H=4, P=64, G=2, N=128, chunk_size=256, act="bf16",
                            seed=911, init="none")
     x, dt, A, Bm, C, D, bias = (dev(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D, s.dt_bias))
