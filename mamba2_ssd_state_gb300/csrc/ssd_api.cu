@@ -65,7 +65,7 @@ size_t gated_norm_ready_bytes(const ssd_scan_args& a, const void* z, const void*
   // the norm's task counter (an int) runs over chunk positions x sequences x groups x
   // parts; chunk positions are at most ceil(T / 128)
   const int64_t positions = ((int64_t)a.T + 127) / 128 * a.nseq;
-  if (positions * (d / group_size) * kReadyParts >= 0x7fffffffLL) return 0;
+  if (positions * (d / group_size) * kReadyParts >= 0x7f000000LL) return 0;  // + the grid
   if (!norm_ready_supported(a.y, z, w, out, (int)d, group_size, a.act_dtype)) return 0;
   if (!scan_tc_ready_plan(a)) return 0;
   return ready_queue_bytes(a.T, a.nseq, (int)(d / group_size));
