@@ -42,7 +42,7 @@ WORKLOAD = "nemotron_h_varlen"
 METRIC = "Mamba2 SSD prefill tokens/s; decode state-update HBM GB/s vs peak"
 KERNEL_CHUNK = 128  # tokens per chunk of the tensor-core scan kernels (their MMA tile)
 SCAN_SRCS = ["scan_tc.cu", "scan_pair.cuh", "tc_ptx.cuh", "ssd_internal.cuh",
-             "scan_segments.cuh"]
+             "scan_segments.cuh", "scan_states.cuh"]
 
 
 def load_peaks():

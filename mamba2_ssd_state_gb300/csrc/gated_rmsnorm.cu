@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(256) norm_ready_kernel(const TA* x,
   __shared__ float part[8];
   __shared__ int red[8];
   __shared__ int task[3];  // sequence (-1: none left), chunk, part * ngroups + group
-  // the chunk-major task list spans max_s(chunks of s) chunk positions of nseq sequences
+  // the chunk-major task list spans max_s(chunks of s) chunk positions of nseq sequences,
+  // taken as nsegm segments of segc positions, position c of every segment before c + 1
   int mine = 0;
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
     const int t0 = cu[s], t1 = cu[s + 1];
@@ -187,7 +188,9 @@ __global__ void __launch_bounds__(256) norm_ready_kernel(const TA* x,
   int maxc = 0;
   for (int k = 0; k < 8; ++k) maxc = max(maxc, red[k]);
   const int per_pos = rq.ngroups * kReadyParts;  // tasks per (chunk, sequence)
-  const long long total = (long long)maxc * nseq * per_pos;
+  const int segc = rq.segc > 0 ? min(rq.segc, max(maxc, 1)) : max(maxc, 1);
+  const int nsegm = (maxc + segc - 1) / segc;
+  const long long total = (long long)segc * nsegm * nseq * per_pos;
   for (;;) {
     if (threadIdx.x == 0) {
       int ts = -1, tc = 0, tk = 0;
@@ -195,7 +198,9 @@ __global__ void __launch_bounds__(256) norm_ready_kernel(const TA* x,
         const long long idx = atomicAdd(rq.head, 1);
         if (idx >= total) break;
         const long long pos = idx / per_pos;
-        const int c = (int)(pos / nseq), s = (int)(pos % nseq);
+        const long long q = pos / nseq;
+        const int s = (int)(pos % nseq);
+        const int c = (int)(q % nsegm) * segc + (int)(q / nsegm);
         const int t0 = cu[s], t1 = cu[s + 1];
         if (!(0 <= t0 && t0 <= t1 && t1 <= T) || c >= (t1 - t0 + 127) / 128) continue;
         ts = s;
@@ -398,7 +403,7 @@ size_t ready_queue_bytes(int64_t T, int nseq, int ngroups) {
   return (bytes + 255) / 256 * 256;
 }
 
-ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs) {
+ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs, int segc) {
   const int64_t nid = (T + 127) / 128 + nseq;
   int* p = static_cast<int*>(ws);
   ReadyQueue rq;
@@ -409,6 +414,7 @@ ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs) {
   rq.ngroups = ngroups;
   rq.gs = gs;
   rq.target = 4 * (gs / 64);
+  rq.segc = segc;
   return rq;
 }
 

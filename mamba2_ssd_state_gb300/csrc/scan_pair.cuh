@@ -34,6 +34,11 @@
 // shared-memory staging, which would add to the traffic of the shared-memory data path
 // the tensor core reads its operands from.  The x buffer of a chunk is released as soon
 // as the epilogue has read x for D x.
+//
+// Split sequences: a CTA may run one segment of segc chunks of a sequence (kSplit).  It
+// enters the segment with the sequence's true state at that point, computed beforehand
+// by the state pass and fold of scan_states.cuh, so its outputs are final and only the
+// sequence's last segment writes the final state.
 
 namespace ssd {
 namespace {
@@ -53,7 +58,8 @@ constexpr int kX = 65536;               // 2 buffers x 2 heads x kTile
 constexpr int kXs = kX + 4 * kTile;     // w o x, 2 heads
 constexpr int kHT = kXs + 2 * kTile;    // h^T bf16, 2 heads: [n rows][64 p]
 constexpr int kPro = kHT + 2 * kTile;   // float [NB][2][kProStride]
-constexpr int kBar = kPro + NB * 2 * kProStride * 4;
+constexpr int kDtR = kPro + NB * 2 * kProStride * 4;  // float [kDtRing][2][QT] dt
+constexpr int kBar = kDtR + kDtRing * 2 * QT * 4;
 constexpr int kNumBar = 2 * 2 + 2 + 2 + 2 * NB + 10;
 constexpr int kFlags = kBar + kNumBar * 8;
 constexpr int kSmemBytes = kFlags + 16 + 1024;
@@ -63,8 +69,10 @@ constexpr uint32_t kColPCB = 0, kColY = 128, kColH = 256, kColO = 384;
 
 }  // namespace pair
 
-// kReady: the unsplit scan of the scan + norm call, which fills the norm's ready queue
-// (a separate instantiation: the queue code costs the plain scan time even unexecuted).
+// kSplit: each CTA runs one segment of a split sequence from the state it enters with
+// (left by scan_state_kernel and scan_fold_kernel, scan_states.cuh).  kReady: the scan of
+// the scan + norm call, which counts finished rows for the norm (a separate instantiation:
+// the counting code costs the plain scan time even unexecuted).
 template <bool kSplit, bool kReady = false>
 __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     scan_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
@@ -105,7 +113,10 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     nseg_s = seg_info[2];
     t0 = seg_info[3];
     t1 = seg_info[4];
-    if (s < 0) return;  // past the batch's last segment
+    if (s < 0) {  // past the batch's last segment
+      griddep_wait();
+      return;
+    }
   } else {
     t0 = prm.cu[s];
     t1 = prm.cu[s + 1];
@@ -114,6 +125,7 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     set_status(prm.status, SSD_DEV_SEQ_META);
   if (!(0 <= t0 && t0 <= t1 && t1 <= prm.T)) {
     if (threadIdx.x == 0) set_status(prm.status, SSD_DEV_SEQ_META);
+    if (kSplit) griddep_wait();
     return;
   }
   const size_t PN = (size_t)P * NSTATE;
@@ -122,20 +134,20 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
   const int nch = kSplit ? max(0, min(prm.segc, nch_s - c0)) : nch_s;
   const int tb = t0 + c0 * QT;
   const int te = min(t1, tb + nch * QT);
-  const bool split = nseg_s > 1;
   // per head: the sign test of A (NaN, +0, -0 fail); a failing head's outputs are zero
   const bool bad0 = !(A0 < 0.f), bad1 = !(A1 < 0.f);
   if ((bad0 || bad1) && threadIdx.x == 0 && pbk == 0 && kseg == 0)
     set_status(prm.status, SSD_DEV_A_NOT_NEG);
-  // the first segment zeroes a failing head's final state (the fix-up kernel skips it)
+  // the first segment zeroes a failing head's final state
   for (int e = 0; e < 2; ++e) {
     if (!(e ? bad1 : bad0) || !prm.fin || kseg != 0) continue;
     float* fin = prm.fin + ((size_t)s * H + h0 + e) * PN + (size_t)p0 * NSTATE;
     for (int i = threadIdx.x; i < PBP * NSTATE; i += pair_threads<kReady>()) fin[i] = 0.f;
   }
   // the scan + norm call: where this CTA's two 64-channel head blocks lie among the norm
-  // groups, and the id of the sequence's first chunk (unsplit: tb is the sequence start)
-  const bool ready = kReady && !kSplit && prm.rq.cnt != nullptr;
+  // groups, and the id of the segment's first chunk (the sequence's chunk ids run from
+  // t0 / 128 + s, and the segment starts c0 chunks in)
+  const bool ready = kReady && prm.rq.cnt != nullptr;
   const int grp0 = ready ? (h0 * P + p0) / prm.rq.gs : 0;
   const int grp1 = ready ? ((h0 + 1) * P + p0) / prm.rq.gs : 0;
   const long long id0 = (long long)(tb / QT) + s;
@@ -160,6 +172,7 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
       if (threadIdx.x == 0)
         for (int cc = 0; cc < nch; ++cc) publish(cc, kPairEpiWarps);
     }
+    if (kSplit) griddep_wait();
     return;
   }
 
@@ -236,16 +249,21 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
       tma_load_3d(sm + kC + 16384, &tmC, c_full, 64, g, tb);
     }
   }
-  // each decay warp's first dt values, loaded during the set-up
-  float dt_first[4] = {0.f, 0.f, 0.f, 0.f};
-  if (warp >= kDecay0 && warp < kMask0 && nch > 0) {
-    const int hh = h0 + (warp - kDecay0);
+  // the decay warps' dt ring (kDtRing chunks in flight); lane l copies and reads tokens
+  // 4 l .. 4 l + 3 of a chunk
+  float* dt_ring = reinterpret_cast<float*>(sm + kDtR);
+  auto fetch_dt = [&](int e, int c) {
+    float* dst = dt_ring + ((c % kDtRing) * 2 + e) * QT + 4 * lane;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int tok = tb + 32 * k + lane;
-      if (tok < t1) dt_first[k] = prm.dt[(size_t)tok * H + hh];
+    for (int u = 0; u < 4; ++u) {
+      const int tok = tb + c * QT + 4 * lane + u;
+      const bool v = c < nch && tok < t1;
+      cp_async4(dst + u, v ? prm.dt + (size_t)tok * H + h0 + e : prm.dt, v);
     }
-  }
+    cp_async_commit();
+  };
+  if (warp >= kDecay0 && warp < kMask0)  // the first chunks, during the set-up
+    for (int c = 0; c < kDtRing; ++c) fetch_dt(warp - kDecay0, c);
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -323,76 +341,24 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
   } else if (warp >= kDecay0 && warp < kMask0) {
     // ------------------------------------------------------------ decay warps (one per head)
     const int e = warp - kDecay0;
-    const int hh = h0 + e;
     const bool bad = e ? bad1 : bad0;
-    const float bias = prm.dt_bias ? prm.dt_bias[hh] : 0.f;
+    const float bias = prm.dt_bias ? prm.dt_bias[h0 + e] : 0.f;
     const float a2 = bad ? 0.f : (e ? A1 : A0) * kLog2e;
-    float dt_raw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) dt_raw[k] = dt_first[k];
-    float* cs_out = (kSplit && split && pbk == 0) ? prm.ws_cs + hh : nullptr;
-    float seg_off = 0.f;
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB;
       if (c >= NB && !wwait(&pro_empty[b], ((c / NB) - 1) & 1)) break;
-      float d[4], cs[4], carry = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = tb + c * QT + 32 * k + lane;
-        const float v0 = dt_raw[k] + bias;
-        d[k] = (tok < t1 && !bad) ? (prm.dt_softplus ? softplus_fast(v0) : v0) : 0.f;
-        float v = d[k] * a2;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float nb = __shfl_up_sync(0xffffffffu, v, off);
-          if (lane >= off) v += nb;
-        }
-        cs[k] = v + carry;
-        carry += __shfl_sync(0xffffffffu, v, 31);
-      }
-      if (c + 1 < nch) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = tb + (c + 1) * QT + 32 * k + lane;
-          dt_raw[k] = tok < t1 ? prm.dt[(size_t)tok * H + hh] : 0.f;
-        }
-      }
-      const float cs_last = carry;
-      if (kSplit && cs_out) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = tb + c * QT + 32 * k + lane;
-          if (tok < t1) cs_out[(size_t)tok * H] = seg_off + cs[k];
-        }
-        seg_off += cs_last;
-      }
-      float* pb = pro + (b * 2 + e) * kProStride;
-      float run_max = -INFINITY;
-      float blk_max[4];
-#pragma unroll
-      for (int k = 3; k >= 0; --k) {
-        float m = cs[k];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        run_max = fmaxf(run_max, m);
-        blk_max[k] = run_max;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int col = 32 * k + lane;
-        const float anchor = __shfl_sync(0xffffffffu, cs[k], 0);
-        float span = anchor - cs[k];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, off));
-        pb[kProCs + col] = cs[k];
-        pb[kProDt + col] = d[k];
-        pb[kProColf + col] = ex2(anchor - cs[k]) * d[k];
-        pb[kProW + col] = ex2(cs_last - cs[k]) * d[k];
-        if (lane == 0)
-          pb[kProSafe + k] =
-              (span <= kFactorLimit && blk_max[k] - anchor <= kFactorLimit) ? 1.f : 0.f;
-      }
+      cp_async_wait<kDtRing - 1>();  // chunk c's copies have landed
+      float raw[4], d[4], cs[4];
+      const float4 r4 =
+          *reinterpret_cast<const float4*>(dt_ring + ((c % kDtRing) * 2 + e) * QT + 4 * lane);
+      raw[0] = r4.x;
+      raw[1] = r4.y;
+      raw[2] = r4.z;
+      raw[3] = r4.w;
+      const float cs_last =
+          chunk_decay(raw, bias, a2, tb + c * QT + 4 * lane, t1, bad, prm.dt_softplus, d, cs);
+      fetch_dt(e, c + kDtRing);  // into the slot just read (its values are in registers)
+      put_decay(pro + (b * 2 + e) * kProStride, d, cs, cs_last);
       __syncwarp();
 #ifdef SSD_FAULT_INJECT
       if (lane == 0 && c != g_inject_withhold_chunk) mbar_arrive(&pro_full[b]);
@@ -400,6 +366,7 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
       if (lane == 0) mbar_arrive(&pro_full[b]);
 #endif
     }
+    cp_async_wait<0>();  // no copy may land after the CTA's shared memory is released
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0)
     if (lane == 0) {
@@ -546,7 +513,9 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
         }
         float v[32];
         tmem_ld32(tmem + lrow + kColPCB + 32 * jb, v);
-        if (jb == q) {  // causal mask on the diagonal block (C.B^T zeroed above it)
+        // column 32 jb + t of row r is kept when t <= tmax (causal)
+        const int tmax = jb < q ? 31 : lane;
+        if (jb == q) {  // C.B^T zeroed above the diagonal (the factorised products stay finite)
 #pragma unroll
           for (int t = 0; t < 32; ++t)
             if (t > lane) v[t] = 0.f;
@@ -555,29 +524,31 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
         for (int e = 0; e < 2; ++e) {
           const float* pb = pro + (b * 2 + e) * kProStride;
           if (pb[kProSafe + jb] != 0.f) {
-            const float rowf = ex2(pb[kProCs + r] - pb[kProCs + 32 * jb]);
+            float rowf[4];
+            mask_row_factors(pb[kProCs + r], pb + kProCs + 32 * jb, rowf);
             const float4* cf = reinterpret_cast<const float4*>(pb + kProColf + 32 * jb);
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 f = cf[e4];
+              const float rf = rowf[e4 >> 1];
               float u0, u1, u2, u3, m0, m1, m2, m3;
-              mul_f32x2(u0, u1, rowf, rowf, f.x, f.y);
-              mul_f32x2(u2, u3, rowf, rowf, f.z, f.w);
+              mul_f32x2(u0, u1, rf, rf, f.x, f.y);
+              mul_f32x2(u2, u3, rf, rf, f.z, f.w);
               mul_f32x2(m0, m1, v[4 * e4 + 0], v[4 * e4 + 1], u0, u1);
               mul_f32x2(m2, m3, v[4 * e4 + 2], v[4 * e4 + 3], u2, u3);
               pk[2 * e4] = pack_bf16(m0, m1);
               pk[2 * e4 + 1] = pack_bf16(m2, m3);
             }
           } else {
-            // the exact decay; cs never increases, so cs_i - cs_j <= 0 wherever j <= i and
-            // the clamp only keeps the masked entries (j > i, zeroed above) finite
+            // the exact decay, one exponential per element (its masked entries may
+            // overflow where cs falls steeply, so they are selected away: 0 * inf is NaN)
             const float cs_i = pb[kProCs + r];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
               const int jt = 32 * jb + 2 * t;
-              const float f0 = ex2(fminf(cs_i - pb[kProCs + jt], 0.f)) * pb[kProDt + jt];
-              const float f1 = ex2(fminf(cs_i - pb[kProCs + jt + 1], 0.f)) * pb[kProDt + jt + 1];
-              pk[t] = pack_bf16(v[2 * t] * f0, v[2 * t + 1] * f1);
+              const float f0 = ex2(cs_i - pb[kProCs + jt]) * pb[kProDt + jt];
+              const float f1 = ex2(cs_i - pb[kProCs + jt + 1]) * pb[kProDt + jt + 1];
+              pk[t] = pack_bf16(2 * t <= tmax ? v[2 * t] * f0 : 0.f, 2 * t + 1 <= tmax ? v[2 * t + 1] * f1 : 0.f);
             }
           }
           tmem_st16(tmem + lrow + kColPCB + 32 * jb + 16 * e, pk);
@@ -597,12 +568,17 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     const int q = warp & 3;
     const int r = 32 * q + lane;           // state row n of h
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
-    const bool has_init =
-        kseg == 0 && prm.init && (prm.has_init == nullptr || prm.has_init[s] != 0);
-    // where the end state of head e goes: the final state, or (split) the segment's local one
+    // the state the chain enters with: the initial state (or zero), or for a later
+    // segment of a split sequence the one the state fold left in the segment before's slot
+    const bool has_init = prm.init && (prm.has_init == nullptr || prm.has_init[s] != 0);
+    const float* entry = kSplit && kseg > 0 ? prm.ws_h + (size_t)(j - 1) * H * PN
+                         : has_init        ? prm.init + (size_t)s * H * PN
+                                           : nullptr;
+    // where the end state of head e goes: the final state, written by a sequence's last
+    // segment (the state pass has the others')
     auto end_state = [&](int e) -> float* {
+      if (kSplit && kseg + 1 < nseg_s) return nullptr;
       const size_t hoff = (size_t)(h0 + e) * PN + (size_t)p0 * NSTATE + r;
-      if (split) return prm.ws_h + (size_t)j * H * PN + hoff;
       return prm.fin ? prm.fin + (size_t)s * H * PN + hoff : nullptr;
     };
     // h^T (bf16, row n = r, 16 channels of head e from `col`) into the shared tile
@@ -636,22 +612,23 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
       for (int e = 0; e < 2; ++e) {
         float* hout = end_state(e);
         if (!hout || (e ? bad1 : bad0)) continue;
-        const float* src = prm.init + ((size_t)s * H + h0 + e) * PN + (size_t)p0 * NSTATE + r;
+        const float* src = entry ? entry + (size_t)(h0 + e) * PN + (size_t)p0 * NSTATE + r : nullptr;
         for (int p = 0; p < PBP; ++p)
-          hout[(size_t)p * NSTATE] = has_init ? src[(size_t)p * NSTATE] : 0.f;
+          hout[(size_t)p * NSTATE] = entry ? src[(size_t)p * NSTATE] : 0.f;
       }
     } else if ((ok = wwait(&pro_full[0], 0))) {
       // the entering state: 2^cs_last(0) h_{-1} into TMEM (the chunk state accumulates onto
       // it), h_{-1}^T in bf16 for Yoff of chunk 0
+      if (kSplit && kseg > 0) griddep_wait();  // the state fold's output
 #pragma unroll 1
       for (int e = 0; e < 2; ++e) {
         const float a0 = ex2(pro[e * kProStride + kProCs + QT - 1]);
-        const float* src = prm.init + ((size_t)s * H + h0 + e) * PN + (size_t)p0 * NSTATE + r;
+        const float* src = entry ? entry + (size_t)(h0 + e) * PN + (size_t)p0 * NSTATE + r : nullptr;
 #pragma unroll 1
         for (int sl = 0; sl < PBP / 16; ++sl) {
           float v[16];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) v[t] = has_init ? src[(size_t)(16 * sl + t) * NSTATE] : 0.f;
+          for (int t = 0; t < 16; ++t) v[t] = entry ? src[(size_t)(16 * sl + t) * NSTATE] : 0.f;
           put_hT(e, 16 * sl, v);
           st_scaled(tmem + lrow + kColH + e * PBP + 16 * sl, a0, v);
         }
@@ -785,6 +762,9 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     set_status(prm.status, SSD_DEV_TIMEOUT);
     if (ready) atomicExch(prm.rq.abort, 1);  // the norm stops waiting for these rows
   }
+  // a split scan's grid ends no earlier than the state passes before it, so that whatever
+  // waits for this grid finds their writes done as well
+  if (kSplit) griddep_wait();
 }
 
 }  // namespace

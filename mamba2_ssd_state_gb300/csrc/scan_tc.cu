@@ -40,9 +40,17 @@
 // what it has in flight and the kernel returns with SSD_DEV_TIMEOUT set.
 //
 // Decay mask arithmetic: exp(cs_i - cs_j) = 2^(cs2_i - cs2_a) * 2^(cs2_a - cs2_j) with the
-// anchor a the first token of j's 32-column block, so the mask costs two multiplies
-// per element instead of an exponential.  The decay warp checks, per block, that both
-// factors stay at most 2^64; a block that fails takes the exact per-element exponential.
+// anchor a the first token of j's 8-token group, so the mask costs two multiplies per
+// element (and four exponentials per row and 32-column block) instead of an exponential.
+// The decay warp checks, per 32-column block, that the factors stay in range (column factors
+// within 2^100, row factors within 2^20); a block that fails takes the exact per-element
+// exponential.  With dt >= 0 only eight tokens decaying by more than
+// 2^100 fail, so strong decays stay on the two-multiply path.
+//
+// The decay warp's lane l owns tokens 4 l .. 4 l + 3 of a chunk: one sequential prefix and
+// one warp scan for the cumulative decay, a few shuffles for the block bounds.  (Its chain
+// of dependent shuffles paces the pipeline when it is long: one scan per 32-token block and
+// full-warp reductions took four times as many.)
 //
 // Few long sequences leave most SMs idle (a chain is one CTA).  The planner may then cut
 // each sequence into segments of segc chunks, every segment its own chain started from a
@@ -78,7 +86,12 @@ constexpr int kDecayWarp = 2 + kMaskWarps + kOutWarps;
 constexpr int kThreads = 32 * (kDecayWarp + 1);
 template <bool kReady> constexpr int tc_threads() { return kThreads; }
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFactorLimit = 64.f;            // log2 bound of a factorised decay factor
+// Log2 bounds of the factorised decay mask: a column factor stays within 2^kColFactorLimit
+// (so a row factor that underflows to zero drops only terms below 2^-26 of the row's own
+// diagonal), a row factor within 2^kRowFactorLimit (its exponent is clamped there, so the
+// rows above a group, whose entries the causal mask zeroes, keep finite products too).
+constexpr float kColFactorLimit = 100.f;
+constexpr float kRowFactorLimit = 20.f;
 constexpr long long kWaitLimit = SSD_WAIT_LIMIT_CYCLES;  // SM cycles a wait may take
 
 #ifdef SSD_FAULT_INJECT
@@ -96,6 +109,10 @@ constexpr uint32_t kColAcc = 192; // Y[2], S, Yoff[2]: PB columns each (5 PB <= 
 // decay buffer: per chunk, float arrays of QT
 constexpr int kProCs = 0, kProDt = QT, kProColf = 2 * QT, kProW = 3 * QT, kProSafe = 4 * QT;
 constexpr int kProStride = 4 * QT + 8;  // floats
+// Chunks of dt in flight per decay warp: copied asynchronously into a shared ring, since
+// a plain load still in flight would hold up the warp's next mbarrier arrive (a release)
+// until it landed.
+constexpr int kDtRing = 4;
 
 struct TcParams {
   const float* dt;
@@ -108,8 +125,10 @@ struct TcParams {
   __nv_bfloat16* y;
   float* fin;
   uint32_t* status;
-  float* ws_h;    // split sequences: local end state per segment [nseg, H, P, N]
-  float* ws_cs;   // split sequences: log2 decay from the segment start to each token [T, H]
+  float* ws_h;    // split sequences: a state per segment [nseg, H, P, N] (one head: the
+                  // segment's local end state; two heads: the state the next one enters with)
+  float* ws_cs;   // split one-head scan: log2 decay from the segment start to each token [T, H]
+  float* ws_d;    // split two-head scan: total log2 decay of each segment [nseg, H]
   int nseq, T, H, P, G, npb, dt_softplus, segc;
   ReadyQueue rq;  // unsplit two-head scan of the scan + norm call: finished rows; cnt NULL = off
 };
@@ -131,7 +150,8 @@ struct Layout {
   static constexpr int kHT = kXs + NXS * kXPad;        // h^T x 2, [N rows][PB] bf16 each
   static constexpr int kHTPad = (NSTATE * kXRow + 1023) / 1024 * 1024;
   static constexpr int kPro = kHT + 2 * kHTPad;        // float [NB][kProStride]
-  static constexpr int kBar = kPro + NB * kProStride * 4;
+  static constexpr int kDtR = kPro + NB * kProStride * 4;  // float [kDtRing][QT] dt
+  static constexpr int kBar = kDtR + kDtRing * QT * 4;
   static constexpr int kNumBar = 2 * NBB + 2 * NBC + 2 * NX + 2 * NB + 12 + 3 * NXS;
   static constexpr int kFlags = kBar + kNumBar * 8;    // abort flag, TMEM base
   static constexpr int kEnd = kFlags + 16;
@@ -151,6 +171,84 @@ __device__ __forceinline__ float softplus_fast(float v) {
   if (v > 20.f) return v;
   const float e = __expf(v);
   return v < -8.f ? e : __logf(1.f + e);
+}
+
+// The decay of one head over one 128-token chunk, by one warp whose lane l owns tokens
+// 4 l .. 4 l + 3: a sequential prefix over its four tokens, then one warp scan of the lane
+// sums (a scan per 32-token column block would put four times the shuffle latency on the
+// warp's chain).  raw = dt of the lane's tokens before the bias; tok0 = the lane's first
+// token.  d = dt after the optional softplus (zero past the sequence end and for a
+// failing head), cs = the inclusive base-2 cumulative decay from the chunk's first token.
+// Returns the chunk's total (the same in every lane).
+__device__ __forceinline__ float chunk_decay(const float (&raw)[4], float bias, float a2,
+                                             int tok0, int t1, bool bad, bool softplus,
+                                             float (&d)[4], float (&cs)[4]) {
+  const int lane = threadIdx.x & 31;
+  float run = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float v0 = raw[u] + bias;
+    d[u] = (tok0 + u < t1 && !bad) ? (softplus ? softplus_fast(v0) : v0) : 0.f;
+    run += d[u] * a2;
+    cs[u] = run;
+  }
+  float incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float nb = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += nb;
+  }
+  float base = __shfl_up_sync(0xffffffffu, incl, 1);  // the sum over the lanes before
+  if (lane == 0) base = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) cs[u] += base;
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// What the mask, state and output roles read of a chunk's decay, from chunk_decay's output
+// (lane l's tokens 4 l .. 4 l + 3) into pb: cs, dt, the mask's column factors
+// 2^(anchor - cs_j) dt_j with the anchor the first token of j's 8-token group, the chunk
+// state's weights 2^(cs_last - cs_j) dt_j, and per 32-column block whether its factorised
+// mask is safe: in each of its 8-token groups the column factors' exponent anchor - cs_j
+// stays within kColFactorLimit and the row factors' largest exponent (the largest cs from
+// the group's first token on, less the anchor) within kRowFactorLimit.  (With dt >= 0 the
+// cumulative decay never increases, so the row factors stay at most 1 and a block fails
+// only where 8 tokens decay by more than 2^kColFactorLimit.)
+__device__ __forceinline__ void put_decay(float* pb, const float (&d)[4], const float (&cs)[4],
+                                          float cs_last) {
+  const int lane = threadIdx.x & 31;
+  const float anchor = __shfl_sync(0xffffffffu, cs[0], lane & ~1);  // lanes 2g, 2g + 1: group g
+  float span = fmaxf(fmaxf(anchor - cs[0], anchor - cs[1]), fmaxf(anchor - cs[2], anchor - cs[3]));
+  float gmax = fmaxf(fmaxf(cs[0], cs[1]), fmaxf(cs[2], cs[3]));
+  span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, 1));
+  gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, 1));
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) {  // the largest cs from the group's first token on
+    const float n = __shfl_down_sync(0xffffffffu, gmax, off);
+    if (lane + off < 32) gmax = fmaxf(gmax, n);
+  }
+  const unsigned safe =
+      __ballot_sync(0xffffffffu, span <= kColFactorLimit && gmax - anchor <= kRowFactorLimit);
+  float cf[4], w[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    cf[u] = ex2(anchor - cs[u]) * d[u];
+    w[u] = ex2(cs_last - cs[u]) * d[u];
+  }
+  *reinterpret_cast<float4*>(pb + kProCs + 4 * lane) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+  *reinterpret_cast<float4*>(pb + kProDt + 4 * lane) = make_float4(d[0], d[1], d[2], d[3]);
+  *reinterpret_cast<float4*>(pb + kProColf + 4 * lane) = make_float4(cf[0], cf[1], cf[2], cf[3]);
+  *reinterpret_cast<float4*>(pb + kProW + 4 * lane) = make_float4(w[0], w[1], w[2], w[3]);
+  if ((lane & 7) == 0)  // block lane / 8: its four groups, lanes lane .. lane + 7
+    pb[kProSafe + (lane >> 3)] = ((safe >> lane) & 0xffu) == 0xffu ? 1.f : 0.f;
+}
+
+// The row factors of the factorised mask of the 32-column block at pbc = pb + kProCs + 32 jb
+// for token row cs_i: 2^(cs_i - anchor) of its four 8-token groups, the exponent clamped to
+// kRowFactorLimit (which only the rows above a group, masked, reach).
+__device__ __forceinline__ void mask_row_factors(float cs_i, const float* pbc, float (&rowf)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) rowf[g] = ex2(fminf(cs_i - pbc[8 * g], kRowFactorLimit));
 }
 
 // kReady: the unsplit scan of the scan + norm call, which fills the norm's ready queue
@@ -324,16 +422,20 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
       tma_load_3d(sm + L::kX, &tmX, &x_full[0], p0, h, tb);
     }
   }
-  // the decay warp's first dt values, loaded during the set-up (strided by H: one sector
-  // per token, a full memory round trip)
-  float dt_first[4] = {0.f, 0.f, 0.f, 0.f};
-  if (warp == kDecayWarp && nch > 0) {
+  // the decay warp's dt ring (kDtRing chunks in flight, the first ones during the set-up);
+  // lane l copies and reads tokens 4 l .. 4 l + 3 of a chunk
+  float* dt_ring = reinterpret_cast<float*>(sm + L::kDtR) + 4 * lane;
+  auto fetch_dt = [&](int c) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int tok = tb + 32 * k + lane;
-      if (tok < t1) dt_first[k] = prm.dt[(size_t)tok * H + h];
+    for (int u = 0; u < 4; ++u) {
+      const int tok = tb + c * QT + 4 * lane + u;
+      const bool v = c < nch && tok < t1;
+      cp_async4(dt_ring + (c % kDtRing) * QT + u, v ? prm.dt + (size_t)tok * H + h : prm.dt, v);
     }
-  }
+    cp_async_commit();
+  };
+  if (warp == kDecayWarp)
+    for (int c = 0; c < kDtRing; ++c) fetch_dt(c);
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -401,74 +503,28 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
     // ------------------------------------------------------------ decay warp
     const float bias = prm.dt_bias ? prm.dt_bias[h] : 0.f;
     const float a2 = Ah * kLog2e;
-    float dt_raw[4];
-    auto load_dt = [&](int c) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = tb + c * QT + 32 * k + lane;
-        dt_raw[k] = tok < t1 ? prm.dt[(size_t)tok * H + h] : 0.f;
-      }
-    };
-#pragma unroll
-    for (int k = 0; k < 4; ++k) dt_raw[k] = dt_first[k];
     // split sequences: each token's log2 decay from its segment start, for the fix-up
     float* cs_out = (kSplit && split && pbk == 0) ? prm.ws_cs + h : nullptr;
     float seg_off = 0.f;
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB;
       if (c >= NB && !wwait(&pro_empty[b], ((c / NB) - 1) & 1)) break;
+      cp_async_wait<kDtRing - 1>();  // chunk c's copies have landed
       // dt, base-2 decay a = dt A log2(e), inclusive cumulative sum over the 128 tokens
-      float d[4], cs[4], carry = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = tb + c * QT + 32 * k + lane;
-        const float v0 = dt_raw[k] + bias;
-        d[k] = tok < t1 ? (prm.dt_softplus ? softplus_fast(v0) : v0) : 0.f;
-        float v = d[k] * a2;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float nb = __shfl_up_sync(0xffffffffu, v, off);
-          if (lane >= off) v += nb;
-        }
-        cs[k] = v + carry;
-        carry += __shfl_sync(0xffffffffu, v, 31);
-      }
-      if (c + 1 < nch) load_dt(c + 1);
-      const float cs_last = carry;
+      const float4 r4 = *reinterpret_cast<const float4*>(dt_ring + (c % kDtRing) * QT);
+      float raw[4] = {r4.x, r4.y, r4.z, r4.w}, d[4], cs[4];
+      const float cs_last =
+          chunk_decay(raw, bias, a2, tb + c * QT + 4 * lane, t1, false, prm.dt_softplus, d, cs);
+      fetch_dt(c + kDtRing);  // into the slot just read (its values are in registers)
       if (kSplit && cs_out) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = tb + c * QT + 32 * k + lane;
-          if (tok < t1) cs_out[(size_t)tok * H] = seg_off + cs[k];
+        for (int u = 0; u < 4; ++u) {
+          const int tok = tb + c * QT + 4 * lane + u;
+          if (tok < t1) cs_out[(size_t)tok * H] = seg_off + cs[u];
         }
         seg_off += cs_last;
       }
-      float* pb = pro + b * kProStride;
-      float run_max = -INFINITY;  // max of cs over blocks >= k (row-factor bound)
-      float blk_max[4];
-#pragma unroll
-      for (int k = 3; k >= 0; --k) {
-        float m = cs[k];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        run_max = fmaxf(run_max, m);
-        blk_max[k] = run_max;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int col = 32 * k + lane;
-        const float anchor = __shfl_sync(0xffffffffu, cs[k], 0);
-        float span = anchor - cs[k];  // column factor exponent
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, off));
-        pb[kProCs + col] = cs[k];
-        pb[kProDt + col] = d[k];
-        pb[kProColf + col] = ex2(anchor - cs[k]) * d[k];
-        pb[kProW + col] = ex2(cs_last - cs[k]) * d[k];
-        if (lane == 0)
-          pb[kProSafe + k] = (span <= kFactorLimit && blk_max[k] - anchor <= kFactorLimit) ? 1.f : 0.f;
-      }
+      put_decay(pro + b * kProStride, d, cs, cs_last);
       __syncwarp();
 #ifdef SSD_FAULT_INJECT
       if (lane == 0 && c != g_inject_withhold_chunk) mbar_arrive(&pro_full[b]);
@@ -476,6 +532,7 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
       if (lane == 0) mbar_arrive(&pro_full[b]);
 #endif
     }
+    cp_async_wait<0>();  // no copy may land after the CTA's shared memory is released
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0)
     if (lane == 0) {
@@ -640,14 +697,16 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
         }
         float* m = v[jj];  // the mask is formed in place of C.B^T
         if (pb[kProSafe + jb] != 0.f) {
-          const float rowf = ex2(cs_i - pb[kProCs + 32 * jb]);
+          float rowf[4];
+          mask_row_factors(cs_i, pb + kProCs + 32 * jb, rowf);
           const float4* cf = reinterpret_cast<const float4*>(pb + kProColf + 32 * jb);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 f = cf[e4];
+            const float rf = rowf[e4 >> 1];
             float t0, t1, t2, t3;  // rowf * colf, then times C.B^T, two lanes at a time
-            mul_f32x2(t0, t1, rowf, rowf, f.x, f.y);
-            mul_f32x2(t2, t3, rowf, rowf, f.z, f.w);
+            mul_f32x2(t0, t1, rf, rf, f.x, f.y);
+            mul_f32x2(t2, t3, rf, rf, f.z, f.w);
             mul_f32x2(m[4 * e4 + 0], m[4 * e4 + 1], m[4 * e4 + 0], m[4 * e4 + 1], t0, t1);
             mul_f32x2(m[4 * e4 + 2], m[4 * e4 + 3], m[4 * e4 + 2], m[4 * e4 + 3], t2, t3);
           }
@@ -814,6 +873,7 @@ namespace {
 }  // namespace ssd
 
 #include "scan_pair.cuh"
+#include "scan_states.cuh"
 
 namespace ssd {
 namespace {
@@ -1224,8 +1284,10 @@ long long seg_capacity(const ssd_scan_args& a, int segc) {
 size_t ws_states_bytes(const ssd_scan_args& a, long long nseg) {
   return (size_t)nseg * a.H * a.P * NSTATE * sizeof(float);
 }
+// The states, then one float per (token, head) (one head per CTA: each token's decay from
+// its segment's start) or per (segment, head) (two heads: each segment's total decay).
 size_t ws_bytes_for(const ssd_scan_args& a, long long nseg) {
-  const size_t cs = (size_t)a.T * a.H * sizeof(float);
+  const size_t cs = (size_t)std::max<long long>(a.T, nseg) * a.H * sizeof(float);
   return (ws_states_bytes(a, nseg) + cs + 255) / 256 * 256;
 }
 
@@ -1244,19 +1306,27 @@ bool pair_ok(const ssd_scan_args& a) {
 
 // Cost model in units of one 128-token chunk of a one-head 64-channel CTA in its steady
 // state (about 2 us).  The host sees only T and nseq (the lengths live on the device),
-// so sequences are taken as equally long.  One CTA per SM; a one-head CTA of channel
-// block PB that runs n chunks costs about kRamp + n (1 + PB/256) (the mask and C.B^T
-// work does not shrink with PB; kRamp is the pipeline fill of its first chunk), a pair
-// CTA kRamp + n kPairChunk for two heads.  A split adds the fix-up grid over the later
-// segments, one CTA per (segment, head, channel block) and one per SM at a time: a fixed
-// cost per wave (its launch, set-up and first tile), one chained step per segment before
-// it (the entering state) and per chunk 0.4 of a scan chunk when up to 96 fix-up CTAs
-// run at once, rising to 1.1 for a wave of 128 or more (each chunk reads and writes a y
-// tile; measured at 24 and at 128 heads).  (kFixBase also carries what a split costs the
-// scan grid itself beyond its chunks.)
+// so sequences are taken as equally long.  One CTA per SM, grids run in waves of one CTA
+// per SM.  A one-head CTA of channel block PB that runs n chunks costs about
+// kRamp + n (1 + PB/256) (the mask and C.B^T work does not shrink with PB; kRamp is the
+// pipeline fill of its first chunk); a pair CTA kPairRamp + n (kPairChunk0 + kPairChunk1 w)
+// for two heads, w the fraction of the SMs its wave occupies (the chunks slow down as more
+// chains share the memory system).  A one-head split adds the fix-up grid over the later
+// segments, one CTA per (segment, head, channel block): a fixed cost per wave (its launch,
+// set-up and first tile), one chained step per segment before it (the entering state) and
+// per chunk 0.4 of a scan chunk when up to 96 fix-up CTAs run at once, rising to 1.1 for a
+// wave of 128 or more (each chunk reads and writes a y tile; measured at 24 and at 128
+// heads).  (kFixBase also carries what a split costs the scan grid itself beyond its
+// chunks.)  A two-head split runs instead, before the scan, the state pass over every
+// segment but a sequence's last (one CTA per segment and head pair, kStateChunk per chunk)
+// and the fold (a fixed cost plus its state traffic, kFoldUnitBytes per unit).  Fitted to
+// one Nemotron-H-shaped sequence of 4K, 16K and 64K tokens, the Nemotron-H varlen batch and
+// Mamba2-130M-shaped batches of 2 x 2K and 1 x 16K tokens, at several segment lengths.
 constexpr double kRamp = 3.0, kFixBase = 5.0, kFixPerSeg = 0.4;
 constexpr double kFixChunkLo = 0.4, kFixChunkHi = 1.1;
-constexpr double kPairChunk = 1.63;  // measured: a pair chunk takes 1.3x a one-head chunk
+constexpr double kPairRamp = 4.0, kPairChunk0 = 1.6, kPairChunk1 = 0.4;
+constexpr double kStateRamp = 1.0, kStateChunk = 0.5, kFoldBase = 5.0;
+constexpr double kFoldUnitBytes = 12e6;
 
 double plan_cost(const ssd_scan_args& a, int hb, int pb, int segc) {
   const int sms = sm_count();
@@ -1267,9 +1337,22 @@ double plan_cost(const ssd_scan_args& a, int hb, int pb, int segc) {
   const long long per_seg = (long long)(a.H / hb) * (a.P / pb);
   const long long ctas = (long long)a.nseq * nseg * per_seg;
   const long long waves = (ctas + sms - 1) / sms;
-  const double per_chunk = hb == 2 ? kPairChunk : 1.0 + pb / 256.0;
-  double cost = (double)waves * (kRamp + chain * per_chunk);
-  if (nseg > 1) {
+  double cost = 0.0;
+  if (hb == 2) {
+    for (long long w = 0; w < waves; ++w) {
+      const double busy = (double)std::min<long long>(sms, ctas - w * sms) / sms;
+      cost += kPairRamp + chain * (kPairChunk0 + kPairChunk1 * busy);
+    }
+  } else {
+    cost = (double)waves * (kRamp + chain * (1.0 + pb / 256.0));
+  }
+  if (nseg > 1 && hb == 2) {
+    const long long st_ctas = (long long)a.nseq * (nseg - 1) * per_seg;
+    const long long st_waves = (st_ctas + sms - 1) / sms;
+    const double fold_bytes =
+        (double)a.nseq * (nseg - 1) * a.H * a.P * NSTATE * 2.0 * sizeof(float);
+    cost += st_waves * (kStateRamp + chain * kStateChunk) + kFoldBase + fold_bytes / kFoldUnitBytes;
+  } else if (nseg > 1) {
     const long long fix_ctas = (long long)a.nseq * (nseg - 1) * a.H * (a.P / pb);
     const long long fix_waves = (fix_ctas + sms - 1) / sms;
     const double busy =
@@ -1282,10 +1365,25 @@ double plan_cost(const ssd_scan_args& a, int hb, int pb, int segc) {
 
 constexpr int kMaxSplitSeqs = 1024;  // each CTA walks the sequence table to find its segment
 
-// The cheapest plan under the cost model.  Splits are considered only when allowed, and
-// only those whose workspace fits in ws_limit bytes.
+// The norm kernel of the overlapped scan + norm starts only once every scan CTA has
+// started, so that form pays only when the scan grid takes at most two waves (one CTA per
+// SM): then the norm runs beside the scan's last wave.  Deeper grids leave it no time.
+constexpr int kReadyMaxWaves = 2;
+
+// A plan the overlapped scan + norm can run: 64-channel blocks, unsplit or split with two
+// heads per CTA (the one-head split's fix-up rewrites y), at most kReadyMaxWaves waves.
+bool ready_eligible(const ssd_scan_args& a, int hb, int pb, int segc) {
+  if (pb != 64 || (segc > 0 && hb != 2)) return false;
+  const long long nseg = segc > 0 ? seg_capacity(a, segc) : a.nseq;
+  return nseg * (a.H / hb) * (a.P / 64) <= (long long)kReadyMaxWaves * sm_count();
+}
+
+// The cheapest plan under the cost model (ready_only: among those the overlapped scan +
+// norm can run).  Splits are considered only when allowed, and only those whose workspace
+// fits in ws_limit bytes.  *cost_out (if given) is the plan's modelled cost.
 bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out,
-               size_t ws_limit = SIZE_MAX) {
+               size_t ws_limit = SIZE_MAX, bool ready_only = false,
+               double* cost_out = nullptr) {
   ScanPlan best;
   double best_cost = 1e300;
   const long long per = ((long long)a.T + a.nseq - 1) / a.nseq;
@@ -1298,6 +1396,7 @@ bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out,
       if (a.P % pb || (a.p_block && a.p_block != pb) || (hb == 2 && pb != 64)) continue;
       auto consider = [&](int segc) {
         if (segc > 0 && ws_bytes_for(a, seg_capacity(a, segc)) > ws_limit) return;
+        if (ready_only && !ready_eligible(a, hb, pb, segc)) return;
         const double c = plan_cost(a, hb, pb, segc);
         if (c < best_cost - 1e-9) {
           best_cost = c;
@@ -1324,6 +1423,7 @@ bool plan_scan(const ssd_scan_args& a, bool allow_split, ScanPlan* out,
   }
   if (best.nseg * (a.H / best.hb) * (a.P / best.pb) > 0x7fffffffLL) return false;
   *out = best;
+  if (cost_out) *cost_out = best_cost;
   return true;
 }
 
@@ -1361,11 +1461,13 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   // dynamic shared memory above 48 KB is opted into once per kernel and device
   static std::atomic<bool> set_one[kMaxDevices], set_one_split[kMaxDevices],
       set_pair[kMaxDevices], set_pair_split[kMaxDevices], set_pair_ready[kMaxDevices],
-      set_one_ready[kMaxDevices], set_fix[kMaxDevices];
+      set_pair_split_ready[kMaxDevices], set_one_ready[kMaxDevices], set_fix[kMaxDevices],
+      set_state[kMaxDevices];
   const bool split = plan.segc > 0;
   bool ok;
   if (pair && rq)
-    ok = opt_in(scan_pair_kernel<false, true>, pair::kSmemBytes, set_pair_ready);
+    ok = split ? opt_in(scan_pair_kernel<true, true>, pair::kSmemBytes, set_pair_split_ready)
+               : opt_in(scan_pair_kernel<false, true>, pair::kSmemBytes, set_pair_ready);
   else if (pair)
     ok = split ? opt_in(scan_pair_kernel<true>, pair::kSmemBytes, set_pair_split)
                : opt_in(scan_pair_kernel<false>, pair::kSmemBytes, set_pair);
@@ -1375,10 +1477,15 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   } else
     ok = split ? opt_in(scan_tc_kernel<PB, true>, L::kSmemBytes, set_one_split)
                : opt_in(scan_tc_kernel<PB, false>, L::kSmemBytes, set_one);
-  if (ok && split) ok = opt_in(scan_fixup_kernel<PB>, FixLayout<PB>::kSmemBytes, set_fix);
+  if (ok && split && pair) ok = opt_in(scan_state_kernel, statepass::kSmemBytes, set_state);
+  if (ok && split && !pair) ok = opt_in(scan_fixup_kernel<PB>, FixLayout<PB>::kSmemBytes, set_fix);
   if (!ok) return SSD_ERR_CUDA;
+  // split workspace: a state per segment, then (one head) every token's log2 decay from
+  // its segment's start or (two heads) every segment's total log2 decay
   float* ws_h = split ? static_cast<float*>(a.workspace) : nullptr;
-  float* ws_cs = split ? ws_h + ws_states_bytes(a, plan.nseg) / sizeof(float) : nullptr;
+  float* ws_tail = split ? ws_h + ws_states_bytes(a, plan.nseg) / sizeof(float) : nullptr;
+  float* ws_cs = pair ? nullptr : ws_tail;
+  float* ws_d = pair ? ws_tail : nullptr;
   TcParams prm;
   prm.dt = a.dt;
   prm.dt_bias = a.dt_bias;
@@ -1392,6 +1499,7 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   prm.status = a.d_status;
   prm.ws_h = ws_h;
   prm.ws_cs = ws_cs;
+  prm.ws_d = ws_d;
   prm.nseq = a.nseq;
   prm.T = a.T;
   prm.H = a.H;
@@ -1402,17 +1510,42 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   prm.segc = plan.segc;
   prm.rq = ReadyQueue{};
   if (rq) {
-    if (split || PB != 64) return SSD_ERR_UNSUPPORTED;
+    if ((split && !pair) || PB != 64) return SSD_ERR_UNSUPPORTED;
     prm.rq = *rq;
   }
   const long long grid = plan.nseg * (a.H / plan.hb) * prm.npb;
+  // programmatic stream serialisation: the grid may start while the one before it drains;
+  // it waits for that grid's completion before it reads what that grid wrote
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  auto pdl_cfg = [&](dim3 g, int threads, int smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = g;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cfg;
+  };
+  if (pair && split) {
+    // the state pass and the fold, then every segment from the state it enters with
+    scan_state_kernel<<<(unsigned)grid, statepass::kThreads, statepass::kSmemBytes, st>>>(mX, mB, prm);
+    if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+    const long long fold_x = ((long long)a.H * a.P * NSTATE / 4 + kFoldThreads - 1) / kFoldThreads;
+    cudaLaunchConfig_t cf = pdl_cfg(dim3((unsigned)fold_x, (unsigned)a.nseq), kFoldThreads, 0);
+    if (cudaLaunchKernelEx(&cf, scan_fold_kernel, prm) != cudaSuccess) return SSD_ERR_CUDA;
+    cudaLaunchConfig_t cs3 = pdl_cfg(dim3((unsigned)grid), pair::kPairThreads, pair::kSmemBytes);
+    const cudaError_t e = rq ? cudaLaunchKernelEx(&cs3, scan_pair_kernel<true, true>, mX, mB, mC, prm)
+                             : cudaLaunchKernelEx(&cs3, scan_pair_kernel<true>, mX, mB, mC, prm);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
   if (pair && rq) {
     scan_pair_kernel<false, true><<<(unsigned)grid, pair::pair_threads<true>(), pair::kSmemBytes, st>>>(mX, mB, mC, prm);
   } else if (pair) {
-    if (split)
-      scan_pair_kernel<true><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
-    else
-      scan_pair_kernel<false><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
+    scan_pair_kernel<false><<<(unsigned)grid, pair::kPairThreads, pair::kSmemBytes, st>>>(mX, mB, mC, prm);
   } else if (rq) {
     if constexpr (PB == 64)
       scan_tc_kernel<PB, false, true><<<(unsigned)grid, tc_threads<true>(), L::kSmemBytes, st>>>(mX, mB, mC, prm);
@@ -1439,18 +1572,10 @@ ssd_status launch_pb(const ssd_scan_args& a, const ScanPlan& plan, cudaStream_t 
   fp.G = a.G;
   fp.npb = prm.npb;
   fp.segc = plan.segc;
-  // programmatic stream serialisation: the fix-up grid may start while the scan grid
-  // drains; it waits for the scan's completion before it reads the scan's outputs
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(plan.nseg * a.H * prm.npb));
-  cfg.blockDim = dim3(kFixThreads);
-  cfg.dynamicSmemBytes = FixLayout<PB>::kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // the fix-up grid may start while the scan grid drains; it waits for the scan's
+  // completion before it reads the scan's outputs
+  cudaLaunchConfig_t cfg =
+      pdl_cfg(dim3((unsigned)(plan.nseg * a.H * prm.npb)), kFixThreads, FixLayout<PB>::kSmemBytes);
   CUtensorMap mY;  // y as the fix-up reads and writes it: tiles of [128 tokens][PB channels]
   if (!make_map(&mY, a.y, a.P, a.H, T, (uint64_t)a.P * 2, (uint64_t)a.H * a.P * 2, PB, QT, xsw))
     return SSD_ERR_CUDA;
@@ -1514,24 +1639,35 @@ ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t st, size_t ws_lim
   return SSD_ERR_UNSUPPORTED;
 }
 
-// The norm kernel of the overlapped form starts only once every scan CTA has started, so
-// the form pays only when the scan grid takes at most two waves (one CTA per SM): then
-// the norm runs beside the scan's last wave.  Deeper grids leave it no time to overlap.
-constexpr int kReadyMaxWaves = 2;
+// The overlapped scan + norm takes the cheapest plan it can run when the cost model puts
+// that plan within kReadySlack of the cheapest plan overall: the norm it hides behind the
+// scan is worth more than the difference.
+constexpr double kReadySlack = 1.15;
 
-bool scan_tc_ready_plan(const ssd_scan_args& a) {
+bool ready_plan(const ssd_scan_args& a, ScanPlan* plan) {
+  ScanPlan all;
+  double c_all = 0.0, c_ready = 0.0;
+  const bool allow = a.seg_chunks >= 0;
+  if (!plan_scan(a, allow, &all, SIZE_MAX, false, &c_all)) return false;
+  if (!plan_scan(a, allow, plan, SIZE_MAX, true, &c_ready)) return false;
+  return c_ready <= kReadySlack * c_all;
+}
+
+bool scan_tc_ready_plan(const ssd_scan_args& a, size_t* split_bytes, int* segc) {
   if (!scan_tc_supported(a)) return false;
   ScanPlan plan;
-  if (final_plan(a, SIZE_MAX, &plan) != SSD_OK || plan.pb != 64 || plan.segc != 0) return false;
-  const long long grid = (long long)a.nseq * (a.H / plan.hb) * (a.P / 64);
-  return grid <= (long long)kReadyMaxWaves * sm_count();
+  if (!ready_plan(a, &plan)) return false;
+  *split_bytes = plan.segc > 0 ? plan.ws_bytes : 0;
+  *segc = plan.segc;
+  return true;
 }
 
 ssd_status launch_scan_tc_ready(const ssd_scan_args& a, const ReadyQueue& rq, cudaStream_t st) {
   ScanPlan plan;
-  const ssd_status v = final_plan(a, SIZE_MAX, &plan);
-  if (v != SSD_OK) return v;
-  if (plan.pb != 64 || plan.segc != 0) return SSD_ERR_UNSUPPORTED;
+  if (!ready_plan(a, &plan) || plan.segc != rq.segc) return SSD_ERR_UNSUPPORTED;
+  if (plan.segc > 0 && !(a.workspace && ((uintptr_t)a.workspace & 255u) == 0 &&
+                         a.workspace_bytes >= plan.ws_bytes))
+    return SSD_ERR_INVALID_ARG;
   return launch_pb<64>(a, plan, st, &rq);
 }
 

@@ -57,18 +57,21 @@ ssd_status validate_update(const ssd_update_args* a) {
 // against 71 at 2048, 93 against 102 at 3072).
 constexpr int32_t kReadyMinTokens = 3072;
 
+// The workspace is the split's (if the plan splits), then the counters.
 size_t gated_norm_ready_bytes(const ssd_scan_args& a, const void* z, const void* w,
-                              int32_t group_size, const void* out) {
+                              int32_t group_size, const void* out, size_t* split_bytes,
+                              int* segc) {
   const int64_t d = (int64_t)a.H * a.P;
   if (a.impl == SSD_IMPL_SIMT || a.act_dtype != SSD_BF16 || group_size % 64 != 0) return 0;
   if (a.T < kReadyMinTokens) return 0;
   // the norm's task counter (an int) runs over chunk positions x sequences x groups x
-  // parts; chunk positions are at most ceil(T / 128)
-  const int64_t positions = ((int64_t)a.T + 127) / 128 * a.nseq;
+  // parts; chunk positions are at most ceil(T / 128), or twice that when split (whole
+  // segments of positions)
+  const int64_t positions = ((int64_t)a.T + 127) / 128 * a.nseq * 2;
   if (positions * (d / group_size) * kReadyParts >= 0x7f000000LL) return 0;  // + the grid
   if (!norm_ready_supported(a.y, z, w, out, (int)d, group_size, a.act_dtype)) return 0;
-  if (!scan_tc_ready_plan(a)) return 0;
-  return ready_queue_bytes(a.T, a.nseq, (int)(d / group_size));
+  if (!scan_tc_ready_plan(a, split_bytes, segc)) return 0;
+  return *split_bytes + ready_queue_bytes(a.T, a.nseq, (int)(d / group_size));
 }
 
 }  // namespace
@@ -138,13 +141,20 @@ ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const void* z,
   if (z && (overlap(z, a.y) || overlap(z, out))) return SSD_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the overlapped form: the norm consumes the scan's finished chunks while it runs
-  const size_t need = gated_norm_ready_bytes(a, z, norm_weight, group_size, out);
+  size_t split_bytes = 0;
+  int segc = 0;
+  const size_t need =
+      gated_norm_ready_bytes(a, z, norm_weight, group_size, out, &split_bytes, &segc);
   if (need > 0 && a.workspace && ((uintptr_t)a.workspace & 255u) == 0 &&
       a.workspace_bytes >= need) {
     const int ngroups = (int)(d / group_size);
-    if (cudaMemsetAsync(a.workspace, 0, need, st) != cudaSuccess) return SSD_ERR_CUDA;
-    const ReadyQueue rq = ready_queue_at(a.workspace, a.T, a.nseq, ngroups, group_size);
-    v = launch_scan_tc_ready(a, rq, st);
+    void* counters = static_cast<char*>(a.workspace) + split_bytes;
+    if (cudaMemsetAsync(counters, 0, need - split_bytes, st) != cudaSuccess) return SSD_ERR_CUDA;
+    const ReadyQueue rq = ready_queue_at(counters, a.T, a.nseq, ngroups, group_size, segc);
+    ssd_scan_args b = a;  // the scan sees the split's part of the workspace only
+    b.workspace = split_bytes ? a.workspace : nullptr;
+    b.workspace_bytes = split_bytes;
+    v = launch_scan_tc_ready(b, rq, st);
     if (v != SSD_OK) return v;
     return launch_norm_ready(a.y, z, norm_weight, out, a.cu_seqlens, a.nseq, a.T, (int)d,
                              group_size, eps, a.act_dtype, weight_dtype, rq, a.d_status,
@@ -169,12 +179,16 @@ size_t ssd_chunk_scan_gated_norm_workspace_size(const ssd_scan_args* args, const
   if (validate_scan(&a) != SSD_OK || a.T == 0 || !norm_weight || !out) return 0;
   const int64_t d = (int64_t)a.H * a.P;
   if (group_size < 1 || d % group_size != 0) return 0;
-  // a split the scan would choose takes the workspace (the norm then follows the scan)
+  // the overlapped form's (its split's and the counters), else a split the scan would
+  // choose (the norm then follows the scan)
   a.workspace = nullptr;
   a.workspace_bytes = 0;
-  const size_t split = a.impl == SSD_IMPL_SIMT ? 0 : scan_tc_workspace_size(a);
-  if (split > 0) return split;
-  return gated_norm_ready_bytes(a, z, norm_weight, group_size, out);
+  size_t split_bytes = 0;
+  int segc = 0;
+  const size_t ready =
+      gated_norm_ready_bytes(a, z, norm_weight, group_size, out, &split_bytes, &segc);
+  if (ready > 0) return ready;
+  return a.impl == SSD_IMPL_SIMT ? 0 : scan_tc_workspace_size(a);
 }
 
 size_t ssd_chunk_scan_workspace_size(const ssd_scan_args* args) {

@@ -43,6 +43,8 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bit) {
 // when its counter reaches 4 per 64-channel block of the group.  The norm kernel takes
 // chunk-groups in chunk-major order (chunk 0 of every sequence, then chunk 1, ...), as
 // kReadyParts tasks of 32 rows, and polls each one's counter before it reads the rows.
+// A split scan runs the segments of a sequence side by side, so there the order is chunk
+// c of every segment of every sequence before chunk c + 1.
 // Chunk ids: chunk c of sequence s (tokens from t0 = cu_seqlens[s]) is floor(t0 / 128) +
 // s + c, distinct for nondecreasing cu_seqlens and below ceil(T / 128) + nseq.
 constexpr int kReadyParts = 4;
@@ -54,6 +56,7 @@ struct ReadyQueue {
   int ngroups;    // norm groups per row
   int gs;         // channels per norm group
   int target;     // contributions that complete a chunk-group: 4 per 64 channels
+  int segc;       // chunks per segment of a split scan (0: unsplit)
 };
 static_assert(128 % kReadyParts == 0, "tasks of whole rows");
 // Count inc contributions to (chunk id, group).  Call after a __threadfence() of every
@@ -67,7 +70,7 @@ __device__ __forceinline__ void ready_count(const ReadyQueue& rq, long long id, 
 // Workspace of the counters for T tokens in nseq sequences (256-byte multiple; zero it
 // before each call), and the counters laid out at ws.
 size_t ready_queue_bytes(int64_t T, int nseq, int ngroups);
-ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs);
+ReadyQueue ready_queue_at(void* ws, int64_t T, int nseq, int ngroups, int gs, int segc);
 
 // Launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_state_update(const ssd_update_args& a, cudaStream_t s);
@@ -94,9 +97,12 @@ cudaError_t launch_norm_ready(const void* x, const void* z, const void* w, void*
 bool scan_tc_supported(const ssd_scan_args& a);
 size_t scan_tc_workspace_size(const ssd_scan_args& a, size_t ws_limit = SIZE_MAX);
 ssd_status launch_scan_tc(const ssd_scan_args& a, cudaStream_t s, size_t ws_limit = SIZE_MAX);
-// True when the call's plan runs the two-head kernel unsplit, the scan that can fill a
-// ReadyQueue; launch_scan_tc_ready launches it so (rq from ready_queue_at).
-bool scan_tc_ready_plan(const ssd_scan_args& a);
+// True when the call's plan (given the workspace it wants) runs a scan that can fill a
+// ReadyQueue: 64-channel blocks, unsplit or split with two heads per CTA, in at most two
+// waves of CTAs.  *split_bytes is then that split's workspace (0: unsplit) and *segc its
+// segment length.  launch_scan_tc_ready launches it so (rq from ready_queue_at; the
+// split's workspace in a.workspace).
+bool scan_tc_ready_plan(const ssd_scan_args& a, size_t* split_bytes, int* segc);
 ssd_status launch_scan_tc_ready(const ssd_scan_args& a, const ReadyQueue& rq, cudaStream_t s);
 
 // Decode-side ops (decode.cu).

@@ -167,6 +167,24 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, in
                : "memory");
 }
 
+// 4-byte asynchronous copy from global to shared memory (zero-filled when !valid).  Its
+// completion is tracked only by the issuing thread's cp.async groups: an mbarrier arrive
+// (a release) does not wait for it, whereas it waits for every earlier plain load of the
+// thread.  So a warp can keep such copies in flight across its handoffs.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of the thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 32-byte global store of eight 32-bit words (one full L2 sector); the address must be
 // 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {

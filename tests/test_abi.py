@@ -131,25 +131,27 @@ def test_scan_workspace_size(lib):
     assert size(nseq=4, T=16384, H=128, G=8, head_block=1) == 0
     auto = size(nseq=1, T=16384)
     assert auto > 0 and auto % 256 == 0
-    # with head pairs allowed, the planner keeps the 6-chunk segments of one head per CTA
-    # for the two 2048-token sequences (its cheapest plan there), and keeps the
-    # Nemotron-H-shaped varlen batch and single 16K / 64K-token Nemotron-H sequences
-    # whole (128 heads: the fix-up of a split would move y twice for every later segment)
-    assert size() == size(head_block=1)
+    # with head pairs allowed, the planner cuts the two 2048-token sequences into 3-chunk
+    # segments of two heads per CTA (13 segments at most: 156 CTAs), keeps the
+    # Nemotron-H-shaped varlen batch and single 16K-token Nemotron-H sequences whole (one
+    # head per CTA there: 128 chains fill the GPU), and cuts a 64K-token one into 64-chunk
+    # segments (9 at most) of two heads per CTA
+    assert size() == r256(13 * 24 * 64 * 128 * 4 + 4096 * 24 * 4)
     assert size(nseq=4, T=16384, H=128, G=8) == 0
     assert size(nseq=1, T=16384, H=128, G=8) == 0
-    assert size(nseq=1, T=65536, H=128, G=8) == 0
+    assert size(nseq=1, T=65536, H=128, G=8) == r256(9 * 128 * 64 * 128 * 4 + 65536 * 128 * 4)
     assert lib.ssd_chunk_scan_workspace_size(None) == 0
 
 
 def test_scan_gated_norm_workspace_size(lib):
-    """Host-side planning only: no kernel runs.  The overlapped scan + norm (two heads per
-    CTA, unsplit, bf16, groups of whole 64-channel head blocks, 16-byte aligned rows, at
-    most two waves of CTAs) wants its ready counters: one int per chunk id (ceil(T/128) +
+    """Host-side planning only: no kernel runs.  The overlapped scan + norm (the
+    tensor-core scan in 64-channel blocks, unsplit or split with two heads per CTA, bf16,
+    groups of whole 64-channel head blocks, 16-byte aligned rows, at most two waves of
+    CTAs) wants its ready counters: one int per chunk id (ceil(T/128) +
     nseq of them) and norm group, plus four ints, rounded up to 256 bytes (norm groups the vector norm takes: 8 x 32 x v channels, v
-    <= 4, and multiples).  A split the planner would choose takes the workspace
-    instead; anything the overlapped form cannot take (or fewer than 3072 tokens) wants
-    none."""
+    <= 4, and multiples).  A two-head split within two waves comes first in the
+    workspace; another split the planner would choose takes the workspace instead;
+    anything the overlapped form cannot take (or fewer than 3072 tokens) wants none."""
     lib.ssd_chunk_scan_gated_norm_workspace_size.argtypes = [
         ctypes.POINTER(ssd.ScanArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
         ctypes.c_void_p]
@@ -177,12 +179,15 @@ def test_scan_gated_norm_workspace_size(lib):
     assert size(z=0x200008) == 0                         # z rows not 16-byte aligned
     assert size(head_block=1) == 0                       # one head per CTA: 512 CTAs
     # a single 16K-token sequence: one head (128 CTAs) or two (64) per CTA both qualify
-    # unsplit; told it may split, the two-head plan splits (the split takes the workspace)
+    # unsplit; told it may split, the two-head plan splits into two segments (192 CTAs
+    # with the segment bound), which the overlapped form takes too: the split's workspace,
+    # then the counters
     assert size(nseq=1, head_block=1) == queue(16384, 1, 8)
+    assert size(nseq=1) == queue(16384, 1, 8)          # the planner's plan: one head
     assert size(nseq=1, head_block=2, seg_chunks=-1) == queue(16384, 1, 8)
     one = dict(kw, nseq=1, head_block=2)
-    assert size(nseq=1, head_block=2) == lib.ssd_chunk_scan_workspace_size(
-        ctypes.byref(_scan_args(**one))) > 0
+    split1 = lib.ssd_chunk_scan_workspace_size(ctypes.byref(_scan_args(**one)))
+    assert split1 > 0 and size(nseq=1, head_block=2) == split1 + queue(16384, 1, 8)
     assert size(nseq=1, head_block=1, p_block=32) == 0   # 32-channel blocks
     assert size(impl=1) == 0                             # SIMT scan
     assert size(act_dtype=ssd.SSD_F32) == 0              # fp32: no tensor-core scan

@@ -403,3 +403,48 @@ def test_split_instance_without_split_sequences():
     yr, fr = scan_oracle(s)
     check_bf16("no-split instance y", y, yr)
     check_bf16("no-split instance final", fs, fr)
+
+
+# The decay mask is factorised per 8-token group (two multiplies per element) where the
+# factors stay within range, and computed exactly per element where they do not.  With
+# the workloads' dt every block takes the factorised form; these cases drive the exact
+# form too.
+MASK_KERNELS = [(64, 1), (0, 2)]
+
+
+@pytest.mark.parametrize("p_block,head_block", MASK_KERNELS)
+def test_strong_decay_takes_both_mask_forms(p_block, head_block):
+    """Heads whose decay over 8 tokens exceeds the factor bound (A down to -4000: the exact
+    form) beside heads far inside it, over ragged sequences."""
+    s = I.make_scan_inputs([700, 129, 1, 300, 385], H=8, P=64, G=2, N=128, chunk_size=128,
+                           act="bf16", seed=601, init="all")
+    s.A = I.Tensor(np.array([-4000.0, -1.0, -300.0, -5.0, -60.0, -2.0, -900.0, -16.0],
+                            dtype=np.float32), "f32")
+    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block, head_block=head_block)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    assert np.isfinite(y).all() and np.isfinite(fs).all()
+    check_bf16(f"strong decay hb={head_block} y", y, yr)
+    check_bf16(f"strong decay hb={head_block} final", fs, fr)
+
+
+@pytest.mark.parametrize("p_block,head_block", MASK_KERNELS)
+def test_plain_dt_with_negative_steps(p_block, head_block):
+    """dt used as given with some negative steps: the cumulative decay rises in places, so
+    both the factorised form's range checks and the exact form see exp(cs_i - cs_j) > 1."""
+    s = I.make_scan_inputs([520, 129, 7, 400], H=4, P=64, G=2, N=128, chunk_size=128,
+                           act="bf16", seed=603, init="all")
+    rng = np.random.default_rng(605)
+    s.dt = I.Tensor((rng.uniform(-0.02, 0.06, size=s.dt.values.shape)).astype(np.float32), "f32")
+    cu = torch.from_numpy(s.cu_seqlens).cuda()
+    status = ssd.new_status()
+    y, fs = ssd.chunk_scan(dev(s.x), dev(s.dt), dev(s.A), dev(s.B), dev(s.C), cu_seqlens=cu,
+                           chunk_size=128, dt_softplus=False, D=dev(s.D),
+                           initial_states=dev(s.initial_states), status=status, impl="tc",
+                           p_block=p_block, head_block=head_block)
+    assert ssd.read_status(status)[1] == 0
+    yr, fr = oracle.scan_seq(s.x.values, s.dt.values, s.A.values, s.B.values, s.C.values,
+                             D=s.D.values, dt_softplus=False,
+                             initial_states=s.initial_states.values, cu_seqlens=s.cu_seqlens)
+    check_bf16(f"negative dt hb={head_block} y", y.float().cpu().numpy(), yr)
+    check_bf16(f"negative dt hb={head_block} final", fs.cpu().numpy(), fr)

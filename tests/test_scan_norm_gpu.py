@@ -410,3 +410,70 @@ def test_overlapped_heads_with_A_not_negative(hb):
     assert torch.equal(out, out_c)
     assert torch.equal(fs, fs_c)
     assert not torch.isnan(out).any()
+
+
+# The overlapped form over a split scan: two heads per CTA, each segment of a sequence run
+# from the state it enters with (state pass, fold, then the scan), so y is written once
+# and counted for the norm.  The workspace is the split's, then the counters.  Held bit for
+# bit to the chained form of the same split (the split's workspace only), to the two plain
+# calls with the same split, and to the oracle.
+SPLIT_OVERLAP_CASES = {
+    "varlen_one_group_of_4_heads": ("varlen_one_group_of_4_heads", 2),
+    "groups_of_4_heads": ("groups_of_4_heads", 3),
+    "p128_head_blocks_in_two_groups": ("p128_head_blocks_in_two_groups", 4),
+    "mamba2_130m_one_group": ("mamba2_130m_one_group", 4),
+}
+
+
+def _split_call(s, n, gs, seg, *, workspace, want_y):
+    d = _dev_inputs(s)
+    T, H, P = d["x"].shape
+    y = _nan((T, H, P), d["x"].dtype) if want_y else None
+    out = _nan((T, H * P), d["x"].dtype)
+    fs = _nan((s.nseq, H, P, s.N), torch.float32)
+    status = ssd.new_status()
+    ssd.chunk_scan_gated_norm(d["x"], d["dt"], d["A"], d["B"], d["C"], dev(n.z), dev(n.weight),
+                              cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size,
+                              group_size=gs, eps=n.eps, D=d["D"], dt_bias=d["dt_bias"],
+                              initial_states=d["initial_states"],
+                              has_initial_state=d["has_initial_state"], y=y, out=out,
+                              final_states=fs, status=status, seg_chunks=seg, head_block=2,
+                              workspace=workspace)
+    _, bits = ssd.read_status(status)
+    return out, y, fs, bits
+
+
+@pytest.mark.parametrize("case", sorted(SPLIT_OVERLAP_CASES))
+@pytest.mark.parametrize("want_y", [True, False])
+def test_overlapped_split_scan_gated_norm(case, want_y):
+    name, seg = SPLIT_OVERLAP_CASES[case]
+    make, gs = OVERLAP_CASES[name]
+    s = make()
+    n = I.make_norm_inputs(s.x.values.shape[0], s.H * s.P, gs, act="bf16", seed=225)
+    d = _dev_inputs(s)
+    T, H, P = d["x"].shape
+    split = ssd.chunk_scan_workspace_size(d["x"], d["B"], d["C"], cu_seqlens=d["cu_seqlens"],
+                                          chunk_size=s.chunk_size, seg_chunks=seg,
+                                          head_block=2)
+    out_t = torch.empty((T, H * P), dtype=d["x"].dtype, device="cuda")
+    nws = ssd.chunk_scan_gated_norm_workspace_size(
+        d["x"], d["B"], d["C"], dev(n.z), dev(n.weight), out_t, cu_seqlens=d["cu_seqlens"],
+        chunk_size=s.chunk_size, group_size=gs, seg_chunks=seg, head_block=2)
+    assert split > 0 and nws == split + _queue_bytes(s, H * P, gs), (split, nws)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    out, y, fs, bits = _split_call(s, n, gs, seg, workspace=ws, want_y=want_y)
+    assert bits == 0
+    ws_c = torch.empty(split, dtype=torch.uint8, device="cuda")   # the chained form
+    out_c, y_c, fs_c, bits_c = _split_call(s, n, gs, seg, workspace=ws_c, want_y=want_y)
+    assert bits_c == 0
+    out_sep, y_sep, fs_sep = _separate(s, n, gs, seg_chunks=seg, head_block=2)
+    assert torch.equal(out, out_c), "overlapped and chained forms differ"
+    assert torch.equal(out, out_sep), "differs from the two plain calls"
+    assert torch.equal(fs, fs_c) and torch.equal(fs, fs_sep)
+    if want_y:
+        assert torch.equal(y, y_c) and torch.equal(y, y_sep)
+    yr, fr, outr = _oracle(s, n, gs)
+    carried = norm_carried_rounding(yr.reshape(T, -1), n.z.values, n.weight.values, gs, n.eps)
+    check_bf16(f"overlapped split {case} out", out.float().cpu().numpy(), outr,
+               stored_bf16=True, carried=carried)
+    check_bf16(f"overlapped split {case} final", fs.cpu().numpy(), fr)
