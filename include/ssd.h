@@ -207,9 +207,10 @@ SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_scan_args* args, ssd_strea
  * Nemotron-H layer path; vt::RmsNormGatedGroup of [vllm.cpp #566]), in one call.
  *
  * Two forms, the same results bit for bit:
- *   - overlapped: when the tensor-core scan runs unsplit in 64-channel blocks with at most
- *     two waves of CTAs (bf16, T >= 3072, group_size a multiple of 64 that the vector
- *     norm takes, 16-byte aligned rows) and args->workspace holds at least
+ *   - overlapped: when the call's scan plan (64-channel blocks, unsplit or split with two
+ *     heads per CTA, at most two waves of CTAs, within 15% of the planner's cheapest plan
+ *     under its cost model) allows it (bf16, T >= 3072, group_size a multiple of 64 that
+ *     the vector norm takes, 16-byte aligned rows) and args->workspace holds at least
  *     ssd_chunk_scan_gated_norm_workspace_size bytes (256-byte aligned; the call zeroes
  *     the bytes it uses, with a memset on the stream), the scan counts every finished
  *     128-token chunk of every norm group in the workspace, and the norm, launched as a
@@ -239,9 +240,11 @@ SSD_API ssd_status ssd_chunk_scan_gated_norm(const ssd_scan_args* args, const vo
 
 /* ------------------------------------------------------------------------------------
  * ssd_chunk_scan_gated_norm_workspace_size -- device workspace (bytes) that
- * ssd_chunk_scan_gated_norm wants for these arguments: the split of the scan when its
- * planner would split (ssd_chunk_scan_workspace_size), else the ready counters of the
- * overlapped form (4 bytes per 128-token chunk and norm group), else 0.  Reads
+ * ssd_chunk_scan_gated_norm wants for these arguments: in the overlapped form, the
+ * workspace of its split (if it splits) then its ready counters (4 bytes per 128-token
+ * chunk and norm group, chunks counted as ceil(T / 128) + nseq, plus 16 bytes, rounded up
+ * to 256); otherwise the split of the scan when its planner would split
+ * (ssd_chunk_scan_workspace_size), else 0.  Reads
  * only shapes, pointers' alignment and the plan inputs of args (no device memory);
  * invalid arguments give 0.  The library does not name a counterpart of this split of
  * the scan + norm call in the source pages: it exists so that the norm may run while the
