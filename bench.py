@@ -557,7 +557,7 @@ def measure_130m(torch, I, ssd, dev, hbm_peak, peak_kind, l2, iters=20):
             "scan_us": sc_ms * 1e3, "scan_split_into_segments": nws > 0,
             "scan_algorithmic_bytes": sb, "scan_achieved_gbs": sb / (sc_ms / 1e3) / 1e9,
             "scan_frac_hbm": sb / (sc_ms / 1e3) / 1e9 / hbm_peak,
-            "scan_traffic": scan_traffic_from_profile("scan_tc_mamba2_130m.md"),
+            "scan_traffic": scan_traffic_from_profile("scan_split_mamba2_130m.md"),
             "peak_kind": f"{peak_kind} hbm copy",
             "note": "median of graph replays, each after an L2 flush"}
 
@@ -753,14 +753,19 @@ def measure_layer_nemotron_h(torch, ssd, dev, hbm_peak, peak_kind, iters=5):
         i = inputs(T)
         out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         fs = torch.empty((len(lens), H, P, N), dtype=torch.float32, device=dev)
-        # the call's workspace: a split's, or the ready counters of its overlapped form
+        # the call's workspace: the overlapped form's (its split's, if any, then the ready
+        # counters), or the split of the chained form's scan, or none
         nws = ssd.chunk_scan_gated_norm_workspace_size(i["x"], i["B"], i["C"], i["z"], wn, out,
                                                        cu_seqlens=cu, chunk_size=128,
                                                        group_size=1024)
         split = ssd.chunk_scan_workspace_size(i["x"], i["B"], i["C"], cu_seqlens=cu,
                                               chunk_size=128)
         ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
-        form = "split" if split > 0 else ("overlapped" if nws > 0 else "chained")
+        counters = (((T + 127) // 128 + len(lens)) * (d // 1024) * 4 + 16 + 255) // 256 * 256
+        if nws > 0 and nws != split:
+            form = "overlapped" if nws == counters else "overlapped, split"
+        else:
+            form = "chained, split" if split > 0 else "chained"
         return T, cu, i, out, fs, ws, form
 
     def timed_flushed(fn, n=iters):

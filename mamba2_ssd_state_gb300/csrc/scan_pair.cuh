@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
   const int grp0 = ready ? (h0 * P + p0) / prm.rq.gs : 0;
   const int grp1 = ready ? ((h0 + 1) * P + p0) / prm.rq.gs : 0;
   const long long id0 = (long long)(tb / QT) + s;
-  // count `per` contributions of each head block to chunk cc (after a __threadfence() of
-  // every thread whose y stores they stand for)
+  // count `per` contributions of each head block to chunk cc (after a barrier with every
+  // thread whose y stores they stand for)
   auto publish = [&](int cc, int per) {
     if (grp0 == grp1) {
       ready_count(prm.rq, id0 + cc, grp0, 2 * per);
@@ -688,11 +688,10 @@ __global__ void __launch_bounds__(pair::pair_threads<kReady>(), 1)
     const uint32_t lrow = (uint32_t)(32 * q) << 16;
     const float D0 = prm.D ? prm.D[h0] : 0.f, D1 = prm.D ? prm.D[h0 + 1] : 0.f;
     const bool wide = ((uintptr_t)prm.y & 31u) == 0;  // 32-byte stores need 32-byte rows
-    // the scan + norm call: this warp's rows of chunk cc are written; make them visible
-    // to the whole GPU and count them (one contribution per head block).  Done one chunk
-    // late, when the stores have long landed, so the fence waits for little.
+    // the scan + norm call: this warp's rows of chunk cc are written; count them (one
+    // contribution per head block), lane 0's release covering the warp's stores.  Done one
+    // chunk late, when the stores have long landed, so the release waits for little.
     auto release_rows = [&](int cc) {
-      __threadfence();
       __syncwarp();
       if (lane == 0) publish(cc, 1);
     };

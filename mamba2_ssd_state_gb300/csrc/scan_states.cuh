@@ -324,19 +324,40 @@ __global__ void __launch_bounds__(kFoldThreads)
   float4 acc = has_init ? *reinterpret_cast<const float4*>(prm.init + (size_t)s * HPN + e4)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
   griddep_wait();  // the local states and decays are the state pass's
+  // the walk is a chain of multiply-adds, but its loads are not: kFoldAhead of them in
+  // flight (the chain's pace would otherwise be one memory round trip per segment)
+  constexpr int kFoldAhead = 4;
   float* slot = prm.ws_h + (size_t)j0 * HPN + e4;
-  float4 l = *reinterpret_cast<const float4*>(slot);
-  for (int k = 0; k + 1 < nseg_s; ++k) {
-    float4 ln = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k + 2 < nseg_s) ln = *reinterpret_cast<const float4*>(slot + HPN);
-    const float dec = ex2(prm.ws_d[(size_t)(j0 + k) * prm.H + h]);
-    acc.x = fmaf(dec, acc.x, l.x);
-    acc.y = fmaf(dec, acc.y, l.y);
-    acc.z = fmaf(dec, acc.z, l.z);
-    acc.w = fmaf(dec, acc.w, l.w);
-    *reinterpret_cast<float4*>(slot) = acc;  // the state segment k + 1 enters with
-    slot += HPN;
-    l = ln;
+  const float* dseg = prm.ws_d + (size_t)j0 * prm.H + h;
+  const int nfold = nseg_s - 1;  // local states to fold: segments 0 .. nseg_s - 2
+  float4 ring[kFoldAhead];
+  float dring[kFoldAhead];
+#pragma unroll
+  for (int k = 0; k < kFoldAhead; ++k) {
+    if (k < nfold) {
+      ring[k] = *reinterpret_cast<const float4*>(slot + (size_t)k * HPN);
+      dring[k] = dseg[(size_t)k * prm.H];
+    }
+  }
+  for (int k0 = 0; k0 < nfold; k0 += kFoldAhead) {
+#pragma unroll
+    for (int u = 0; u < kFoldAhead; ++u) {
+      const int k = k0 + u;
+      if (k < nfold) {
+        const float4 l = ring[u];
+        const float dec = ex2(dring[u]);
+        if (k + kFoldAhead < nfold) {  // the load kFoldAhead segments on
+          ring[u] = *reinterpret_cast<const float4*>(slot + (size_t)(k + kFoldAhead) * HPN);
+          dring[u] = dseg[(size_t)(k + kFoldAhead) * prm.H];
+        }
+        acc.x = fmaf(dec, acc.x, l.x);
+        acc.y = fmaf(dec, acc.y, l.y);
+        acc.z = fmaf(dec, acc.z, l.z);
+        acc.w = fmaf(dec, acc.w, l.w);
+        // the state segment k + 1 enters with, over segment k's local one (already read)
+        *reinterpret_cast<float4*>(slot + (size_t)k * HPN) = acc;
+      }
+    }
   }
 }
 

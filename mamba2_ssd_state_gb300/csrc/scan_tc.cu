@@ -769,10 +769,10 @@ __global__ void __launch_bounds__(tc_threads<kReady>(), 1)
     };
     write_hT(1);
     const float Dh = prm.D ? prm.D[h] : 0.f;
-    // the scan + norm call: this warp's rows of chunk cc are written; make them visible to
-    // the whole GPU and count them.  Done one chunk late, when the stores have long landed.
+    // the scan + norm call: this warp's rows of chunk cc are written; count them, lane 0's
+    // release covering the warp's stores.  Done one chunk late, when the stores have long
+    // landed.
     auto release_rows = [&](int cc) {
-      __threadfence();
       __syncwarp();
       if (lane == 0) ready_count(prm.rq, id0 + cc, grp, 1);
     };
@@ -1324,8 +1324,8 @@ bool pair_ok(const ssd_scan_args& a) {
 // Mamba2-130M-shaped batches of 2 x 2K and 1 x 16K tokens, at several segment lengths.
 constexpr double kRamp = 3.0, kFixBase = 5.0, kFixPerSeg = 0.4;
 constexpr double kFixChunkLo = 0.4, kFixChunkHi = 1.1;
-constexpr double kPairRamp = 4.0, kPairChunk0 = 1.6, kPairChunk1 = 0.4;
-constexpr double kStateRamp = 1.0, kStateChunk = 0.5, kFoldBase = 5.0;
+constexpr double kPairRamp = 3.0, kPairChunk0 = 1.5, kPairChunk1 = 0.4;
+constexpr double kStateRamp = 1.0, kStateChunk = 0.7, kFoldBase = 3.0;
 constexpr double kFoldUnitBytes = 12e6;
 
 double plan_cost(const ssd_scan_args& a, int hb, int pb, int segc) {

@@ -39,8 +39,9 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bit) {
 // so that the norm runs while the scan still works on later chunks.  For every 128-token
 // chunk of every sequence and every norm group there is a counter: each output warp of
 // the scan, once its 32 rows of one 64-channel head block of a chunk are written and
-// fenced, adds one to it (a reduction nobody waits for), so a chunk-group is complete
-// when its counter reaches 4 per 64-channel block of the group.  The norm kernel takes
+// ordered by a warp barrier, adds one to it (a release reduction nobody waits for), so a
+// chunk-group is complete when its counter reaches 4 per 64-channel block of the group.
+// The norm kernel takes
 // chunk-groups in chunk-major order (chunk 0 of every sequence, then chunk 1, ...), as
 // kReadyParts tasks of 32 rows, and polls each one's counter before it reads the rows.
 // A split scan runs the segments of a sequence side by side, so there the order is chunk
@@ -59,13 +60,16 @@ struct ReadyQueue {
   int segc;       // chunks per segment of a split scan (0: unsplit)
 };
 static_assert(128 % kReadyParts == 0, "tasks of whole rows");
-// Count inc contributions to (chunk id, group).  Call after a __threadfence() of every
-// thread whose stores they stand for (and a warp or block barrier between those threads
-// and the caller).
+// Count inc contributions to (chunk id, group): a reduction with release semantics at GPU
+// scope (nobody waits for it).  Call after a warp or block barrier with every thread whose
+// stores the contributions stand for: the barrier orders their stores before the caller's
+// release, and a release carries what was ordered before it, so a reader that sees the
+// count (and then fences) sees the stores.
 __device__ __forceinline__ void ready_count(const ReadyQueue& rq, long long id, int grp,
                                             int inc) {
   if (id < 0 || id >= rq.nid) return;  // only for cu_seqlens that are not nondecreasing
-  atomicAdd(rq.cnt + id * rq.ngroups + grp, inc);  // result unused: a reduction
+  int* p = rq.cnt + id * rq.ngroups + grp;
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(inc) : "memory");
 }
 // Workspace of the counters for T tokens in nseq sequences (256-byte multiple; zero it
 // before each call), and the counters laid out at ws.

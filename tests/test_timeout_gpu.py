@@ -110,12 +110,14 @@ def test_withheld_chunk_times_out_and_context_survives(fault_lib):
     check_bf16("after timeout final", f_gpu, f_ref)
 
 
-@pytest.mark.parametrize("hb", [1, 2])
-def test_overlapped_norm_stops_waiting_when_the_scan_aborts(fault_lib, hb):
+@pytest.mark.parametrize("hb,seg", [(1, -1), (2, -1), (2, 8)])
+def test_overlapped_norm_stops_waiting_when_the_scan_aborts(fault_lib, hb, seg):
     """The scan + norm call in its overlapped form (the norm drains a queue the scan fills
     as it runs): when the scan gives up on a withheld chunk, it raises the queue's abort
     flag, the norm's blocks stop waiting for the chunks that will not come, and the call
-    ends with SSD_DEV_TIMEOUT on a context that still runs the regular library."""
+    ends with SSD_DEV_TIMEOUT on a context that still runs the regular library.  With
+    seg = 8 the scan is a two-head split (state pass, fold, then every segment from its
+    entering state: each segment's chunk 1 is withheld)."""
     # 4 heads (two head pairs), one norm group over their 256 channels; 4200 tokens (the
     # overlapped form needs at least 3072)
     s = I.make_scan_inputs([4200], H=4, P=64, G=2, N=128, chunk_size=256, act="bf16",
@@ -129,12 +131,16 @@ def test_overlapped_norm_stops_waiting_when_the_scan_aborts(fault_lib, hb):
     fs = torch.zeros((s.nseq, s.H, s.P, s.N), device="cuda")
     status = ssd.new_status()
     a = scan_args_struct(x, dt, A, Bm, C, cu, s.chunk_size, D=D, dt_bias=bias, fs=fs,
-                         status=status, seg_chunks=-1, head_block=hb)
+                         status=status, seg_chunks=seg, head_block=hb)
     a.impl, a.p_block = 2, 64
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
     nws = fault_lib.ssd_chunk_scan_gated_norm_workspace_size(ctypes.byref(a), ptr(z), ptr(w),
                                                             d, ptr(out))
     assert nws > 0, "the case must take the overlapped form"
+    if seg > 0:  # the split's part comes first, then the ready counters
+        split = ssd.chunk_scan_workspace_size(x, Bm, C, cu_seqlens=cu, chunk_size=s.chunk_size,
+                                              seg_chunks=seg, head_block=hb, p_block=64)
+        assert 0 < split < nws
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     a.workspace, a.workspace_bytes = ws.data_ptr(), nws
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -153,9 +159,9 @@ def test_overlapped_norm_stops_waiting_when_the_scan_aborts(fault_lib, hb):
     # the same context: the regular library's overlapped call equals its plain calls
     out2, _ = ssd.chunk_scan_gated_norm(x, dt, A, Bm, C, z, w, cu_seqlens=cu,
                                         chunk_size=s.chunk_size, group_size=d, D=D,
-                                        dt_bias=bias, seg_chunks=-1, head_block=hb, p_block=64)
+                                        dt_bias=bias, seg_chunks=seg, head_block=hb, p_block=64)
     y_sep, _ = ssd.chunk_scan(x, dt, A, Bm, C, cu_seqlens=cu, chunk_size=s.chunk_size, D=D,
-                              dt_bias=bias, seg_chunks=-1, head_block=hb, p_block=64)
+                              dt_bias=bias, seg_chunks=seg, head_block=hb, p_block=64)
     out_sep = ssd.gated_rmsnorm(y_sep.view(T, d), z, w, group_size=d)
     torch.cuda.synchronize()
     assert torch.equal(out2, out_sep)
