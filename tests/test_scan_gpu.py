@@ -448,3 +448,45 @@ def test_plain_dt_with_negative_steps(p_block, head_block):
                              initial_states=s.initial_states.values, cu_seqlens=s.cu_seqlens)
     check_bf16(f"negative dt hb={head_block} y", y.float().cpu().numpy(), yr)
     check_bf16(f"negative dt hb={head_block} final", fs.cpu().numpy(), fr)
+
+
+@pytest.mark.parametrize("seg", [1, 2, 5])
+def test_pair_split_headdim_128_groups(seg):
+    """The two-head split at P = 128 (two 64-channel blocks per head pair: the state pass,
+    the fold and the scan each run per block) and G = 2 (two head pairs per group), with
+    sequences of whole segments, a partial last segment, one token and none."""
+    s = I.make_scan_inputs([640, 77, 1, 0, 513, 1280], H=8, P=128, G=2, N=128, chunk_size=128,
+                           act="bf16", seed=613, init=[1, 0, 1, 1, 0, 1])
+    y, fs, bits = scan_gpu(s, impl="tc", head_block=2, seg_chunks=seg)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16(f"pair split P=128 seg={seg} y", y, yr)
+    check_bf16(f"pair split P=128 seg={seg} final", fs, fr)
+    np.testing.assert_array_equal(fs[3], s.initial_states.values[3])  # the empty sequence
+
+
+def test_pair_split_without_D_and_final_states():
+    """The two-head split with no D and no final states (the last segment writes nothing,
+    the state pass and the fold still carry every later segment's entering state)."""
+    s = I.make_scan_inputs([900, 300], H=4, P=64, G=1, N=128, chunk_size=256, act="bf16",
+                           seed=617, init="all")
+    y, fs, bits = scan_gpu(s, impl="tc", head_block=2, seg_chunks=2, final=False, D=False)
+    assert bits == 0 and fs is None
+    yr, _ = scan_oracle(s, D=False)
+    check_bf16("pair split no D y", y, yr)
+
+
+def test_pair_split_long_segments():
+    """Segments of 12 chunks: the state pass's rings (3 TMA stages, 8 weight slots, 4 dt
+    chunks) wrap several times within a segment; a 25-chunk sequence gives two whole
+    segments and a one-chunk last one."""
+    s = I.make_scan_inputs([3100, 200], H=4, P=64, G=2, N=128, chunk_size=128, act="bf16",
+                           seed=619, init=[1, 1])
+    y, fs, bits = scan_gpu(s, impl="tc", head_block=2, seg_chunks=12)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    check_bf16("pair split seg=12 y", y, yr)
+    check_bf16("pair split seg=12 final", fs, fr)
+    y1, f1, _ = scan_gpu(s, impl="tc", head_block=2, seg_chunks=-1)
+    check_bf16("pair split seg=12 vs unsplit y", y, y1)
+    check_bf16("pair split seg=12 vs unsplit final", fs, f1)
