@@ -160,14 +160,19 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream
  * for these arguments; 0 when it will not split sequences.
  *
  * The tensor-core path may split a sequence into segments of seg_chunks 128-token chunks
- * so that more chains run in parallel: each segment is scanned from a zero state, the
- * segment end states are chained afterwards (h_in(k+1) = exp(sum of dt A over segment k)
- * h_in(k) + local end state of k), and y of every later segment receives the
- * exp(cumulative decay) C h_in^T term it was missing.  The result is the same chunked
- * evaluation of the recurrence, regrouped.  The workspace holds one fp32 [H, P, N] state
- * per segment and one fp32 decay per token and head; it is caller-owned device memory of at least the returned size, 256-byte
- * aligned, passed in args->workspace / workspace_bytes, and its contents need not be
- * initialised.  With no or too small a workspace and seg_chunks = 0 the scan runs
+ * so that more chains run in parallel.  Every segment's entering state is
+ * h_in(k+1) = exp(sum of dt A over segment k) h_in(k) + L(k), with L(k) the state segment k
+ * leaves when entered with zero.  With two heads per CTA, a state pass computes L(k) and
+ * the decay of every segment but a sequence's last, a fold chains them into each entering
+ * state, and every segment is then scanned from its entering state (three launches, y
+ * written once).  With one head per CTA, each segment is scanned from a zero state and y of
+ * every later segment then receives the exp(cumulative decay) C h_in^T term it was missing
+ * (two launches).  Either way the result is the same chunked evaluation of the
+ * recurrence, regrouped.  The workspace holds one fp32 [H, P, N] state per segment, then
+ * one fp32 value per token (one head per CTA: its decay from the segment start) or per
+ * segment (two heads: the segment's total decay) and head, max(T, segments) x H floats;
+ * it is caller-owned device memory of at least the returned size, 256-byte aligned,
+ * passed in args->workspace / workspace_bytes, and its contents need not be initialised.  With no or too small a workspace and seg_chunks = 0 the scan runs
  * without splitting.  A sequence has at most 64 segments (a longer segment length is
  * used where seg_chunks would give more).
  *   seg_chunks: 0 = choose (needs the workspace); -1 = never split; k >= 1 = split into
