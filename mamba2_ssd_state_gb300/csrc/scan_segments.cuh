@@ -55,4 +55,41 @@ __device__ inline bool find_segment_warp(const int32_t* cu, int nseq, int segc, 
   return false;
 }
 
+// The scheduling order of an unsplit scan grid: slot j (the j-th group of a sequence's
+// CTAs in the grid) runs the j-th longest sequence by chunk count, ties in index order (the
+// longest-processing-time-first rule).  The longest chain of chunks sets the scan's time
+// when it starts late: in batch order, a long sequence packed after short ones starts only
+// as they finish.  Batches of more than kLptMaxSeqs sequences fill many waves, where the
+// order hardly moves the tail: they run in batch order.  Every warp of the CTA calls it and
+// gets the sequence and its token range [t0, t1) in all lanes, from one load per lane and 32
+// shuffles (no shared memory, no block barrier).  Malformed lengths rank as empty; the
+// caller checks the range it gets.
+constexpr int kLptMaxSeqs = 32;
+__device__ inline void lpt_sequence_warp(const int32_t* cu, int nseq, int T, int j, int& s,
+                                         int& t0, int& t1) {
+  if (nseq <= 1 || nseq > kLptMaxSeqs) {
+    s = j;
+    t0 = cu[j];
+    t1 = cu[j + 1];
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  int a = 0, b = 0, n = -1;  // past the batch: below every sequence
+  if (lane < nseq) {
+    a = cu[lane];
+    b = cu[lane + 1];
+    n = (0 <= a && a <= b && b <= T) ? (b - a + kScanChunk - 1) / kScanChunk : 0;
+  }
+  int rank = 0;  // sequences ahead of this lane's in the order
+#pragma unroll
+  for (int src = 0; src < 32; ++src) {
+    const int o = __shfl_sync(0xffffffffu, n, src);
+    rank += (o > n || (o == n && src < lane)) ? 1 : 0;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < nseq && rank == j);
+  s = hit ? __ffs(hit) - 1 : j;  // ranks are a permutation of 0..nseq-1: always a hit
+  t0 = __shfl_sync(0xffffffffu, a, s & 31);
+  t1 = __shfl_sync(0xffffffffu, b, s & 31);
+}
+
 }  // namespace ssd

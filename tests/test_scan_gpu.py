@@ -490,3 +490,24 @@ def test_pair_split_long_segments():
     y1, f1, _ = scan_gpu(s, impl="tc", head_block=2, seg_chunks=-1)
     check_bf16("pair split seg=12 vs unsplit y", y, y1)
     check_bf16("pair split seg=12 vs unsplit final", fs, f1)
+
+
+@pytest.mark.parametrize("p_block,head_block", [(64, 1), (64, 2)])
+@pytest.mark.parametrize("nseq", [2, 31, 32, 33])
+def test_longest_first_slot_order(p_block, head_block, nseq):
+    """Packed sequences in ascending length, with runs of equal lengths and empty ones: an
+    unsplit grid of up to 32 sequences runs them longest first, so every slot maps to another
+    sequence and ties break by index; 33 sequences keep batch order."""
+    rng = np.random.default_rng(521 + nseq)
+    lens = np.sort(rng.choice([0, 1, 100, 128, 129, 256, 300, 513], size=nseq))
+    init = (rng.random(nseq) < 0.5).astype(int).tolist()
+    s = I.make_scan_inputs(lens.tolist(), H=2, P=64, G=1, N=128, chunk_size=128, act="bf16",
+                           seed=523, init=init)
+    y, fs, bits = scan_gpu(s, impl="tc", p_block=p_block, head_block=head_block, seg_chunks=0)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    tag = f"{nseq} ascending seqs pb={p_block} hb={head_block}"
+    check_bf16(f"{tag} y", y, yr)
+    check_bf16(f"{tag} final", fs, fr)
+    empty = np.flatnonzero(lens == 0)
+    np.testing.assert_array_equal(fs[empty], s.initial_states.values[empty])

@@ -271,6 +271,13 @@ OVERLAP_CASES = {
                                    act="bf16", seed=215, init="all"), 256),
     # one group over all 1536 channels of the Mamba2-130M shape: 12 CTAs per group
     "mamba2_130m_one_group": (lambda: I.scan_workload("mamba2_130m"), 1536),
+    # two longest sequences of equal length, neither first: the plain scan of the two-call
+    # comparison runs its grid longest first, the overlapped form in batch order, and the
+    # outputs agree bit for bit
+    "tied_longest_not_first": (
+        lambda: I.make_scan_inputs([513, 2300, 64, 2300, 0, 1], H=16, P=64, G=2, N=128,
+                                   chunk_size=128, act="bf16", seed=219,
+                                   init=[1, 0, 1, 1, 0, 1]), 256),
 }
 
 
