@@ -948,19 +948,38 @@ def profile_only(args):
         dtype = torch.bfloat16 if t.dtype == "bf16" else torch.float32
         return torch.from_numpy(np.ascontiguousarray(t.values)).to(dev, dtype)
 
-    if args.profile in ("scan", "scan_large", "scan_split", "norm", "norm_large"):
+    if args.profile in ("scan", "scan_large", "scan_split", "norm", "norm_large", "layer_16k"):
         name = ("mamba2_130m" if args.profile in ("scan", "norm", "scan_split")
                 else "nemotron_h_varlen")
-        # scan_split: one 16384-token sequence, which the planner cuts into segments
-        s = (I.scan_workload(name, seqlens=[16384]) if args.profile == "scan_split"
-             else I.scan_workload(name))
+        # scan_split: one 16384-token sequence, which the planner cuts into segments;
+        # layer_16k: one Nemotron-H-shaped sequence of 16384 tokens through the scan + norm
+        # call (the form the layer sweep times)
+        if args.profile == "scan_split":
+            s = I.scan_workload(name, seqlens=[16384])
+        elif args.profile == "layer_16k":
+            s = I.scan_workload(name, seqlens=[16384], init="all")
+        else:
+            s = I.scan_workload(name)
         x, dt, A, B, C, Dp, bias, init = (T_(t) for t in (s.x, s.dt, s.A, s.B, s.C, s.D,
                                                             s.dt_bias, s.initial_states))
         hi = torch.from_numpy(s.has_initial_state).to(dev)
         cu = torch.from_numpy(s.cu_seqlens).to(dev)
         y = torch.empty_like(x)
         fs = torch.empty((s.nseq, s.H, s.P, s.N), dtype=torch.float32, device=dev)
-        if args.profile in ("norm", "norm_large"):
+        if args.profile == "layer_16k":
+            w = I.WORKLOADS[name]
+            nrm = I.make_norm_inputs(s.T, s.H * s.P, w["norm_group"], act="bf16", seed=w["seed"] + 50)
+            z, wt = T_(nrm.z), T_(nrm.weight)
+            out = torch.empty((s.T, s.H * s.P), dtype=torch.bfloat16, device=dev)
+            nws = ssd.chunk_scan_gated_norm_workspace_size(x, B, C, z, wt, out, cu_seqlens=cu,
+                                                           chunk_size=s.chunk_size,
+                                                           group_size=w["norm_group"])
+            ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+            run = lambda: ssd.chunk_scan_gated_norm(  # noqa
+                x, dt, A, B, C, z, wt, cu_seqlens=cu, chunk_size=s.chunk_size,
+                group_size=w["norm_group"], D=Dp, dt_bias=bias, initial_states=init,
+                has_initial_state=hi, final_states=fs, out=out, workspace=ws)
+        elif args.profile in ("norm", "norm_large"):
             w = I.WORKLOADS[name]
             nrm = I.make_norm_inputs(s.T, s.H * s.P, w["norm_group"], act="bf16", seed=w["seed"] + 50)
             z, wt = T_(nrm.z), T_(nrm.weight)
@@ -1008,7 +1027,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / large-scan legs")
     ap.add_argument("--profile", choices=["scan", "scan_large", "scan_split", "norm", "norm_large",
-                                          "update", "multi", "copy"],
+                                          "layer_16k", "update", "multi", "copy"],
                     help="only launch this op's benchmark workload steps times (for ncu)")
     args = ap.parse_args()
     if args.profile:
