@@ -123,6 +123,8 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  *   d_status: uint32 device word or NULL
  * Shapes: H % G == 0; SIMT path N <= 256; tensor-core path bf16, N == 128,
  * P % 16 == 0, 16-byte aligned rows.  Outputs must not alias inputs.
+ * The order of the sequences in the batch does not change the results; an unsplit
+ * tensor-core scan of 2 to 32 sequences starts the longest ones first.
  * ------------------------------------------------------------------------------------ */
 typedef struct {
   uint32_t struct_size;
@@ -172,8 +174,8 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_scan_args* args, ssd_stream_t stream
  * one fp32 value per token (one head per CTA: its decay from the segment start) or per
  * segment (two heads: the segment's total decay) and head, max(T, segments) x H floats;
  * it is caller-owned device memory of at least the returned size, 256-byte aligned,
- * passed in args->workspace / workspace_bytes, and its contents need not be initialised.  With no or too small a workspace and seg_chunks = 0 the scan runs
- * without splitting.  A sequence has at most 64 segments (a longer segment length is
+ * passed in args->workspace / workspace_bytes, and its contents need not be initialised.
+ * With no or too small a workspace and seg_chunks = 0 the scan runs without splitting.  A sequence has at most 64 segments (a longer segment length is
  * used where seg_chunks would give more).
  *   seg_chunks: 0 = choose (needs the workspace); -1 = never split; k >= 1 = split into
  *   segments of k chunks (SSD_ERR_INVALID_ARG if the workspace is missing or too small).
