@@ -516,3 +516,33 @@ def test_layer_single_65536_full_size():
     ref = oracle.gated_rmsnorm(yrows, n.z.values[rows], n.weight.values, group_size=gs,
                                eps=n.eps)
     check_bf16("layer 65536 out rows", out.float().cpu().numpy()[rows], ref, stored_bf16=True)
+
+
+def test_layer_nemotron_h_varlen_full_size():
+    """The benchmark's headline call at full size: the 4 packed sequences (8192, 3000, 517,
+    4675), H=128, G=8, initial states on sequences 0 and 2, norm groups of 1024, through the
+    form the library plans (the overlapped one).  y and the final states of every head
+    against the oracle, and `out` on rows of every sequence against the oracle's gated norm
+    of the call's own y."""
+    from gpu_util import scan_oracle
+    s = I.scan_workload("nemotron_h_varlen")
+    T, gs = s.T, 1024
+    n = I.make_norm_inputs(T, 128 * 64, gs, act="bf16", seed=235)
+    d = _dev_inputs(s)
+    nws = ssd.chunk_scan_gated_norm_workspace_size(
+        d["x"], d["B"], d["C"], dev(n.z), dev(n.weight),
+        torch.empty((T, 128 * 64), dtype=torch.bfloat16, device="cuda"),
+        cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size, group_size=gs)
+    assert nws == _queue_bytes(s, 128 * 64, gs), f"not the overlapped form (workspace {nws})"
+    del d
+    out, y, fs, bits = _fused(s, n, gs, want_y=True)
+    assert bits == 0
+    yr, fr = scan_oracle(s)
+    yg = y.float().cpu().numpy()
+    check_bf16("headline call y", yg, yr, stored_bf16=True)
+    check_bf16("headline call final", fs.cpu().numpy(), fr)
+    rows = np.concatenate([np.arange(a, b, 61) for a, b in zip(s.cu_seqlens[:-1], s.cu_seqlens[1:])])
+    yrows = yg[rows].reshape(len(rows), -1)
+    ref = oracle.gated_rmsnorm(yrows, n.z.values[rows], n.weight.values, group_size=gs,
+                               eps=n.eps)
+    check_bf16("headline call out rows", out.float().cpu().numpy()[rows], ref, stored_bf16=True)
