@@ -6,6 +6,8 @@ Each case is held to the bar against the oracle's composition (scan, then gated 
 and, bit for bit, to ssd_chunk_scan followed by gated_rmsnorm as two plain calls.  The
 outputs start as NaN, so a norm that read y before the scan had written it would show.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -546,3 +548,62 @@ def test_layer_nemotron_h_varlen_full_size():
     ref = oracle.gated_rmsnorm(yrows, n.z.values[rows], n.weight.values, group_size=gs,
                                eps=n.eps)
     check_bf16("headline call out rows", out.float().cpu().numpy()[rows], ref, stored_bf16=True)
+
+
+def test_layer_mixed_64_prefills_full_size():
+    """The mixed layer batch the benchmark times, at full size: 64 packed prefills of
+    128..4096 tokens (133 547 tokens), H=128, P=64, G=8, N=128, initial states on every other
+    sequence, norm groups of 1024, through the call as the library plans it (a grid of 28
+    waves: the chained form).  Inputs are drawn on the device in the workloads'
+    distributions (2 GB each of x and z: too slow to draw on the host in a test) and the
+    oracle reads them back.  y and the final states of heads from four groups against the
+    oracle, and `out` on rows of every sequence against the oracle's gated norm of the call's
+    own y."""
+    lens = np.random.default_rng(4243).integers(128, 4097, size=64)
+    T, H, P, G, N, gs = int(lens.sum()), 128, 64, 8, 128, 1024
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(237)
+    bf = torch.bfloat16
+
+    def randn(*shape):
+        return torch.randn(shape, generator=gen, device="cuda")
+
+    x = randn(T, H, P).to(bf)
+    dt = randn(T, H)
+    A = -torch.exp(torch.rand(H, generator=gen, device="cuda") * math.log(16.0))
+    u = torch.rand(H, generator=gen, device="cuda") * (0.1 - 1e-3) + 1e-3
+    bias = torch.log(torch.expm1(u))
+    Dp = randn(H)
+    B = (randn(T, G, N) / math.sqrt(N)).to(bf)
+    C = (randn(T, G, N) / math.sqrt(N)).to(bf)
+    init = 0.1 * randn(64, H, P, N)
+    hi = torch.tensor([1, 0] * 32, dtype=torch.uint8, device="cuda")
+    z = randn(T, H * P).to(bf)
+    w = (1 + 0.1 * randn(H * P)).to(bf)
+    y = _nan((T, H, P), bf)
+    out = _nan((T, H * P), bf)
+    fs = _nan((64, H, P, N), torch.float32)
+    status = ssd.new_status()
+    ssd.chunk_scan_gated_norm(x, dt, A, B, C, z, w, cu_seqlens=torch.from_numpy(cu).cuda(),
+                              chunk_size=128, group_size=gs, eps=1e-5, D=Dp, dt_bias=bias,
+                              initial_states=init, has_initial_state=hi, y=y, out=out,
+                              final_states=fs, status=status)
+    _, bits = ssd.read_status(status)
+    assert bits == 0
+    heads = np.array([0, 37, 64, 127])
+    g = heads // (H // G)
+    th = torch.from_numpy(heads).cuda()
+    tg = torch.from_numpy(g).cuda()
+    host = lambda t: t.float().cpu().numpy()  # noqa: E731
+    yr, fr = oracle.scan_seq(host(x[:, th]), host(dt[:, th]), host(A[th]), host(B[:, tg]),
+                             host(C[:, tg]), D=host(Dp[th]), dt_bias=host(bias[th]),
+                             initial_states=host(init[:, th]), has_initial_state=hi.cpu().numpy(),
+                             cu_seqlens=cu)
+    check_bf16("mixed 64 y", host(y[:, th]), yr, stored_bf16=True)
+    check_bf16("mixed 64 final", host(fs[:, th]), fr)
+    rows = torch.from_numpy(np.concatenate([np.arange(a, b, 211) for a, b in
+                                            zip(cu[:-1], cu[1:])])).cuda()
+    ref = oracle.gated_rmsnorm(host(y[rows]).reshape(len(rows), -1), host(z[rows]), host(w),
+                               group_size=gs, eps=1e-5)
+    check_bf16("mixed 64 out rows", host(out[rows]), ref, stored_bf16=True)
