@@ -488,14 +488,16 @@ def test_overlapped_split_scan_gated_norm(case, want_y):
     check_bf16(f"overlapped split {case} final", fs.cpu().numpy(), fr)
 
 
-def test_layer_single_65536_full_size():
-    """The largest single-sequence layer call the benchmark times: one 65 536-token
-    sequence, H=128, P=64, G=8, N=128, an initial state, norm groups of 1024, through the
-    form the library plans for it (the overlapped one).  y and the final states of heads
-    from four groups against the oracle; `out` on rows across the sequence against the
-    oracle's gated norm of the call's own y (a property that holds at any size)."""
+@pytest.mark.parametrize("L", [1024, 4096, 16384, 65536])
+def test_layer_single_sequence_full_size(L):
+    """The single-sequence layer calls the benchmark times: one sequence of L tokens,
+    H=128, P=64, G=8, N=128, an initial state, norm groups of 1024, through the form the
+    library plans for it (chained at 1024 tokens, overlapped from 4096).  y and the final
+    states of heads from four groups against the oracle; `out` on rows across the sequence
+    against the oracle's gated norm of the call's own y (a property that holds at any
+    size)."""
     from gpu_util import scan_oracle
-    s = I.make_scan_inputs([65536], H=128, P=64, G=8, N=128, chunk_size=128, act="bf16",
+    s = I.make_scan_inputs([L], H=128, P=64, G=8, N=128, chunk_size=128, act="bf16",
                            seed=231, init="all")
     T, gs = s.T, 1024
     n = I.make_norm_inputs(T, 128 * 64, gs, act="bf16", seed=233)
@@ -504,20 +506,21 @@ def test_layer_single_65536_full_size():
         d["x"], d["B"], d["C"], dev(n.z), dev(n.weight),
         torch.empty((T, 128 * 64), dtype=torch.bfloat16, device="cuda"),
         cu_seqlens=d["cu_seqlens"], chunk_size=s.chunk_size, group_size=gs)
-    assert nws == _queue_bytes(s, 128 * 64, gs), f"not the overlapped form (workspace {nws})"
+    overlapped = nws == _queue_bytes(s, 128 * 64, gs)
+    assert overlapped == (L >= 4096), f"L={L}: workspace {nws}"
     del d
     out, y, fs, bits = _fused(s, n, gs, want_y=True)
     assert bits == 0
     heads = [0, 37, 64, 127]
     yr, fr = scan_oracle(s, heads=heads)
     yg = y.float().cpu().numpy()
-    check_bf16("layer 65536 y", yg[:, heads], yr, stored_bf16=True)
-    check_bf16("layer 65536 final", fs[:, heads].cpu().numpy(), fr)
-    rows = np.arange(0, T, 997)
+    check_bf16(f"layer {L} y", yg[:, heads], yr, stored_bf16=True)
+    check_bf16(f"layer {L} final", fs[:, heads].cpu().numpy(), fr)
+    rows = np.arange(0, T, 997 if L > 4096 else 61)
     yrows = yg[rows].reshape(len(rows), -1)
     ref = oracle.gated_rmsnorm(yrows, n.z.values[rows], n.weight.values, group_size=gs,
                                eps=n.eps)
-    check_bf16("layer 65536 out rows", out.float().cpu().numpy()[rows], ref, stored_bf16=True)
+    check_bf16(f"layer {L} out rows", out.float().cpu().numpy()[rows], ref, stored_bf16=True)
 
 
 def test_layer_nemotron_h_varlen_full_size():
