@@ -598,6 +598,38 @@ def measure_extra(torch, I, ssd, dev, hbm_peak, peak_kind, iters=20):
         "algorithmic_bytes_per_launch": ub, "achieved_gbs": ub / (us / 1e6) / 1e9,
         "peak_gbs": hbm_peak, "frac": ub / (us / 1e6) / 1e9 / hbm_peak,
         "peak_kind": f"{peak_kind} hbm copy"}
+    # the batch sweep of the decode workload (1, 32, 128 and 256 requests, 10 % of the rows
+    # -1): one graph-replayed call after each L2 flush, so that small batches, whose states
+    # would otherwise stay in L2 from one call to the next, read and write HBM
+    l2 = L2Flush(torch, dev)
+    sweep = {}
+    for b in (1, 32, 128, 256):
+        ib = I.padded_permutation(S, b, seed=3000 + b)
+        ubi = I.make_update_inputs(1, ib, H, P, G, N, act="bf16", seed=3100 + b,
+                                   pool_values=np.zeros((1, H, P, N), np.float32))
+        ab = (pool, torch.from_numpy(ib).to(dev), T_(ubi.x), T_(ubi.dt), T_(ubi.A), T_(ubi.B),
+              T_(ubi.C))
+        kwb = dict(D=T_(ubi.D), dt_bias=T_(ubi.dt_bias))
+        ssd.state_update(*ab, **kwb)
+        g = graph_of(torch, lambda: ssd.state_update(*ab, **kwb))
+        ts = []
+        for _ in range(11):
+            l2.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        usb = float(np.median(ts))
+        act = int((ib >= 0).sum())
+        byb = update_bytes(act, b, H, P, G, N)
+        sweep[str(b)] = {"active_slots": act, "us": usb, "achieved_gbs": byb / (usb / 1e6) / 1e9,
+                         "frac": byb / (usb / 1e6) / 1e9 / hbm_peak}
+    res["decode_state_update_sweep"] = {
+        "workload": "512-slot pool of [128,64,128] fp32 states, batch 1 / 32 / 128 / 256, 10% "
+                    "rows -1; each call graph-replayed after an L2 flush (latency of one call, "
+                    "launch included)", "by_batch": sweep, "peak_kind": f"{peak_kind} hbm copy"}
     # decode layer step (update + D + gated norm, 8 norm groups of 1024) on the same
     # pool and batch, against the two calls made separately
     z = torch.randn((batch, H * P), device=dev).to(torch.bfloat16)
